@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark: the sparse-attention decode step on one GB300 (or N replicas).
+
+One step = one decode step of every layer of the workload: indexer + top-k,
+LRU ensure + miss fetch from the pinned host mirror, remap, sparse paged
+attention (+ split merge), all layers of the range in one launch per stage.
+
+Default workload: 4 requests x 12 layers, 65,536 tokens each in 64-token
+pages, fp8 e4m3 K/V with per-token scales, 16/2 heads, top-32, a pool of 320
+GPU slots per layer over a pinned host mirror, queries on a rho = 0.8 random
+walk (frequent misses).  Inputs are seeded synthetic data resident in HBM
+before timing; L2 is flushed (256 MiB write) between timed steps.
+
+Timing: per stage a captured CUDA graph, CUDA events between stages on the
+launching stream; W warm-up steps, then K timed steps.  `e2e` repeats the
+metric through the public API (DecodeRunner.step) with the step's queries
+copied from pinned host memory and its output copied back inside the timed
+region.  Multi-GPU (torchrun): each rank runs an independent replica (the
+path shards by request with no collective): weak scaling, max time over ranks.
+
+--impl reference times the plain CPU oracle on the host cores on a bounded
+sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "sparse decode layer-steps/s (x batch)"
+UNIT = "layer-steps/s"
+DEFAULT_WORKLOAD = "lru_pressure_64k_fp8"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="bound on the timed oracle sample")
+    return ap.parse_args()
+
+
+def get_workload(name: str) -> wl.Workload:
+    if name in wl.WORKLOADS:
+        return wl.WORKLOADS[name]
+    if name.startswith("sweep_"):
+        # sweep_<bf16|fp8>_<resident|20pct>_b<B>
+        _, kv, res, b = name.split("_")
+        return wl.sweep_workload(int(b[1:]), kv == "fp8", 1.0 if res == "resident" else 0.2)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the method must move; the dense KV it skips is not
+# counted, nor any re-read or split-K partial)
+# ---------------------------------------------------------------------------
+
+def n_selected(w: wl.Workload) -> np.ndarray:
+    n_b = np.ceil(w.lens / w.page_size).astype(np.int64)
+    return np.minimum(n_b, w.block_topk + 1)
+
+
+def decode_bytes(w: wl.Workload) -> int:
+    """Per launch of the attention over all layers: the selected pages' K and V
+    (one KV head each, per KV head), fp8 per-token scales, q, out, sel, phys."""
+    esz = 1 if w.fp8 else 2
+    ns = n_selected(w)
+    kv = int(ns.sum()) * w.n_kv_heads * 2 * w.page_size * w.head_dim * esz
+    sc = int(ns.sum()) * w.page_size * 8 if w.fp8 else 0
+    qo = 2 * w.batch * w.n_q_heads * w.head_dim * 2
+    lists = 2 * w.batch * (2 * w.block_topk + 8) * 4
+    return w.n_layers * (kv + sc + qo + lists)
+
+
+def index_bytes(w: wl.Workload) -> int:
+    """The slab scan: int8 page keys of every page of every request, plus the
+    block-table ids and q."""
+    n_b = np.ceil(w.lens / w.page_size).astype(np.int64)
+    per_layer = int(n_b.sum()) * (w.n_kv_heads * w.head_dim + 4) + \
+        w.batch * w.n_q_heads * w.head_dim * 2
+    return w.n_layers * per_layer
+
+
+def page_fetch_bytes(w: wl.Workload) -> int:
+    esz = 1 if w.fp8 else 2
+    b = 2 * w.n_kv_heads * w.page_size * w.head_dim * esz
+    return b + (2 * w.page_size * 4 if w.fp8 else 0)
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (reported baseline; also --impl reference)
+# ---------------------------------------------------------------------------
+
+def cpu_oracle_sample(w: wl.Workload, seconds: float):
+    import oracle
+    oracle.build()
+    lay = oracle.OracleLayout(w.page_size, w.n_q_heads, w.n_kv_heads, w.head_dim, w.fp8,
+                              w.n_layers, w.logical_pages, w.slots, w.batch,
+                              w.pages_per_request, w.block_topk)
+    one = wl.Workload(**{**w.__dict__, "n_layers": 1})
+    lay.n_layers = 1
+    orc = oracle.OracleKV(lay, host_tier=w.host_tier, identity=not w.host_tier)
+    k, v, pos = wl.store_batch(one, 0)
+    orc.store(0, k, v, pos)
+    qs = wl.queries(one.with_(steps=max(w.steps, 64)) if w.rho is not None else one, 0)
+    bt = wl.block_table(w)
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        orc.step(0, qs[steps % len(qs)], bt, w.lens)
+        steps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    value = steps * w.batch / dt
+    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"layer 0 of {w.name}, all {w.batch} requests, {steps} decode steps "
+                      f"(index, select, ensure+copy, remap, fp64 attention), single thread, "
+                      f"{dt:.1f} s; prefill not timed"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def build_runner(w: wl.Workload, rank: int):
+    import torch
+    from sparse_attention_decode_indexer_gb300 import Layout
+    from sparse_attention_decode_indexer_gb300.runner import DecodeRunner
+    lay = Layout(w.page_size, w.n_q_heads, w.n_kv_heads, w.head_dim, w.fp8, w.n_layers,
+                 w.logical_pages, w.slots, w.batch, w.pages_per_request, w.block_topk)
+    run = DecodeRunner(lay, host_tier=w.host_tier, identity=not w.host_tier,
+                       block_table=wl.block_table(w), seq_lens=w.lens)
+    for l in range(w.n_layers):
+        k, v, pos = wl.store_batch(w, l)
+        kd = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).cuda()[None]
+        vd = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda()[None]
+        run.store(l, 1, kd, vd, torch.from_numpy(pos).cuda())
+        del kd, vd
+    torch.cuda.synchronize()
+    st = int(run.status.item())
+    if st != 0:
+        raise RuntimeError(f"store status {st}")
+    return run
+
+
+def queries_all(w: wl.Workload, n_steps: int):
+    """[n_steps][L][B][Hq][D] bf16 bit patterns of the query walk."""
+    ww = w.with_(steps=n_steps)
+    return np.stack([wl.queries(ww, l) for l in range(w.n_layers)], axis=1)
+
+
+def h2d_peak_gbs(torch) -> float:
+    n = 256 << 20
+    src = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        best = max(best, n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    return best
+
+
+def run_ours(args, rank: int, world: int, dist):
+    import torch
+    import sparse_attention_decode_indexer_gb300 as ssa
+
+    w = get_workload(args.workload)
+    if world > 1:
+        w = w.with_(seed=w.seed + 1000 * rank)     # an independent replica per rank
+    W, K = args.warmup, args.steps
+    run = build_runner(w, rank)
+    n_total = W + 3 * K
+    q_np = queries_all(w, n_total)
+    q_all = torch.from_numpy(q_np.view(np.int16)).view(torch.bfloat16).cuda()
+    q_cur = q_all[0].clone()
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")   # 256 MiB > L2
+    L = w.n_layers
+    c = run.cache
+
+    def st_index():
+        ssa.ssa_index_topk(c, 0, L, q_cur, run.block_table, run.seq_lens, run.sel, run.n_sel,
+                           None, run.status, run.ws)
+
+    def st_ensure():
+        ssa.ssa_ensure_resident(c, 0, L, run.sel, run.block_table, run.miss_page, run.miss_slot,
+                                run.n_miss, run.status, run.ws)
+
+    def st_remap():
+        ssa.ssa_remap_block_table(c, 0, L, run.sel, run.block_table, run.phys, run.status)
+
+    def st_decode():
+        ssa.ssa_sparse_paged_decode(c, 0, L, q_cur, run.sel, run.phys, run.seq_lens,
+                                    run.sm_scale, run.out, run.status, run.ws)
+
+    stages = [("index_topk", st_index), ("ensure", st_ensure), ("remap", st_remap),
+              ("decode", st_decode)]
+    # one eager step (function attributes, lazy init), then capture each stage
+    for _, f in stages:
+        f()
+    torch.cuda.synchronize()
+    graphs = []
+    launches_per_step = 0
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    for name, f in stages:
+        g = torch.cuda.CUDAGraph()
+        n0 = ssa.launch_count()
+        with torch.cuda.graph(g, stream=s):
+            f()
+        launches_per_step += ssa.launch_count() - n0
+        graphs.append(g)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    # the eager step above advanced the LRU state by one step: restart cleanly
+    ssa.ssa_lru_init(c, identity=not w.host_tier)
+    for l in range(L):
+        k, v, pos = wl.store_batch(w, l)
+        kd = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).cuda()[None]
+        vd = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda()[None]
+        run.store(l, 1, kd, vd, torch.from_numpy(pos).cuda())
+    miss_acc = torch.zeros(L, dtype=torch.int64, device="cuda")
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+          for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for t in range(W + K):
+        flush.zero_()
+        q_cur.copy_(q_all[t])
+        timed = t >= W
+        if timed:
+            ev[t - W][0].record()
+        for i, g in enumerate(graphs):
+            g.replay()
+            if timed:
+                ev[t - W][i + 1].record()
+        if timed:
+            miss_acc += run.n_miss
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    st = int(run.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {ssa.status_str(st)}")
+    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
+    stage_ms = {name: [e[i].elapsed_time(e[i + 1]) for e in ev] for i, (name, _) in
+                enumerate(stages)}
+    total_s = sum(step_ms) * 1e-3
+    if dist:
+        tt = torch.tensor([total_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_s = float(tt.item())
+    units = L * w.batch * K * world
+    value = units / total_s
+    misses = int(miss_acc.sum().item())
+
+    # per-layer launches (4 calls per layer, layer after layer), one graph per step
+    g_pl = torch.cuda.CUDAGraph()
+    run.step(q_cur, per_layer=True)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_pl, stream=s):
+        run.step(q_cur, per_layer=True)
+    torch.cuda.synchronize()
+    pl_ms = []
+    for t in range(K):
+        flush.zero_()
+        q_cur.copy_(q_all[W + K + t])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g_pl.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        pl_ms.append(e0.elapsed_time(e1))
+
+    # end to end through the public API, host buffers in and out
+    e2e = None
+    if not args.no_e2e:
+        q_host = torch.from_numpy(q_np[W + 2 * K:W + 3 * K].view(np.int16)).view(
+            torch.bfloat16).pin_memory()
+        out_host = torch.empty((K,) + tuple(run.out.shape), dtype=torch.bfloat16,
+                               pin_memory=True)
+        q_dev = torch.empty_like(q_cur)
+        e2e_ms = []
+        for t in range(K):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            q_dev.copy_(q_host[t], non_blocking=True)
+            out = run.step(q_dev)
+            out_host[t].copy_(out, non_blocking=True)
+            e1.record()
+            e1.synchronize()
+            e2e_ms.append(e0.elapsed_time(e1))
+        tot = sum(e2e_ms) * 1e-3
+        if dist:
+            tt = torch.tensor([tot], dtype=torch.float64, device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            tot = float(tt.item())
+        e2e = {"value": units / tot, "unit": UNIT,
+               "h2d_bytes_per_step": int(q_host[0].numel() * 2),
+               "d2h_bytes_per_step": int(out_host[0].numel() * 2),
+               "ms_per_step": 1e3 * tot / K,
+               "path": "DecodeRunner.step (4 C-ABI calls, direct launches) + pinned H2D q / D2H out"}
+
+    if rank != 0:
+        return None
+    peak, peak_kind = load_peaks()
+    dec_ms = statistics.mean(stage_ms["decode"])
+    dec_bytes = decode_bytes(w)
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    idx_ms = statistics.mean(stage_ms["index_topk"])
+    ens_ms = statistics.mean(stage_ms["ensure"])
+    miss_bytes = misses * page_fetch_bytes(w) / K
+    h2d = h2d_peak_gbs(torch)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": 1e3 * total_s / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 codes, f16 tensor-core MMA, f32 accumulate; int8 indexer" if w.fp8 else
+                 "bf16 tensor-core MMA, f32 accumulate; int8 indexer",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "layers": w.n_layers, "ctx": w.ctx,
+                   "page_size": w.page_size, "heads": f"{w.n_q_heads}/{w.n_kv_heads}",
+                   "head_dim": w.head_dim, "kv": "fp8_e4m3" if w.fp8 else "bf16",
+                   "block_topk": w.block_topk, "pool_slots": w.slots,
+                   "host_tier": w.host_tier, "layers_per_launch": w.n_layers,
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "timing": "per-stage CUDA graphs, CUDA events on the launching stream"},
+        "roofline": {"kernel": "ssa_sparse_paged_decode (decode_kernel + merge_kernel)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"hbm_gbs of {peak_kind}",
+                     "traffic": None, "alg_bytes_per_launch": dec_bytes,
+                     "avg_launch_us": 1e3 * dec_ms},
+        "stages_us": {k: 1e3 * statistics.mean(v) for k, v in stage_ms.items()},
+        "index_roofline": {"alg_bytes": index_bytes(w),
+                           "achieved_gbs": index_bytes(w) / (idx_ms * 1e-3) / 1e9},
+        "miss": {"pages_per_step": misses / K, "bytes_per_step": miss_bytes,
+                 "gbs_over_ensure_stage": miss_bytes / (ens_ms * 1e-3) / 1e9,
+                 "h2d_copy_engine_peak_gbs": h2d},
+        "per_layer_sequential": {"value": L * w.batch * K / (sum(pl_ms) * 1e-3),
+                                 "ms_per_step": statistics.mean(pl_ms),
+                                 "note": "4 calls per layer, layer after layer, one graph"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    return line, w
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = get_workload(args.workload)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = cpu_oracle_sample(w, args.cpu_seconds * max(1, min(args.steps, 5)) / 5)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64 attention, int32 indexer", "data": "synthetic",
+                "config": {"workload": w.name}, "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    res = run_ours(args, rank, world, dist)
+    if rank == 0:
+        line, w = res
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_seconds)
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

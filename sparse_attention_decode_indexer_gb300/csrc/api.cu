@@ -1,0 +1,287 @@
+// api.cu -- the C ABI: argument checks, workspace layout, launches.
+//
+// Every entry point validates its arguments on the host, then only enqueues
+// kernels on the caller's stream.  Nothing here synchronises, allocates or
+// keeps a pointer past the call.
+#include <climits>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+
+namespace ssa {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+thread_local long long g_launches = 0;
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return SSA_ERR_CUDA;
+}
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Validate the layout and fill the derived view.
+int check_layout(const ssa_layout* lay, Dims& d) {
+  if (!lay) return SSA_ERR_INVALID_ARG;
+  d.P = lay->page_size; d.Hq = lay->n_q_heads; d.Hkv = lay->n_kv_heads; d.D = lay->head_dim;
+  d.fp8 = lay->kv_dtype == SSA_KV_FP8_E4M3;
+  d.Lyr = lay->n_layers; d.Lp = lay->logical_pages; d.S = lay->pool_slots;
+  d.B = lay->batch; d.nmax = lay->max_pages; d.k = lay->block_topk; d.W = lay->max_sel;
+  if (d.Lyr < 1 || d.Lp < 1 || d.S < 1 || d.B < 1 || d.nmax < 1 || d.k < 1 || d.Hq < 1 ||
+      d.Hkv < 1)
+    return SSA_ERR_INVALID_ARG;
+  if (d.W != 2 * d.k + 8) return SSA_ERR_INVALID_ARG;
+  if (lay->kv_dtype != SSA_KV_BF16 && lay->kv_dtype != SSA_KV_FP8_E4M3) return SSA_ERR_UNSUPPORTED;
+  if (d.D != 128) return SSA_ERR_UNSUPPORTED;
+  if (!(d.P == 16 || d.P == 32 || d.P == 64 || d.P == 128)) return SSA_ERR_UNSUPPORTED;
+  if (d.Hq % d.Hkv != 0) return SSA_ERR_UNSUPPORTED;
+  d.G = d.Hq / d.Hkv;
+  if (d.G > 8) return SSA_ERR_UNSUPPORTED;
+  if (!pow2(d.Hkv) || d.Hkv > 8) return SSA_ERR_UNSUPPORTED;
+  // TMA coordinates are int32: every row index of the pool must fit
+  const long long rows = (long long)d.Lyr * d.S * d.Hkv * (d.P > d.D ? d.P : d.D);
+  if (rows >= INT_MAX) return SSA_ERR_UNSUPPORTED;
+  if ((long long)d.B * d.W > 16384) return SSA_ERR_UNSUPPORTED;   // ensure sorts in shared memory
+  if (d.nmax > 49152) return SSA_ERR_UNSUPPORTED;                  // select keeps scores in smem
+  return SSA_OK;
+}
+
+int check_range(const Dims& d, int layer0, int n_layers) {
+  if (layer0 < 0 || n_layers < 1 || layer0 + n_layers > d.Lyr) return SSA_ERR_INVALID_ARG;
+  return SSA_OK;
+}
+
+bool has_mirror(const Dims& d, const ssa_cache* c) {
+  if (d.fp8)
+    return c->k_mirror && c->v_mirror && c->k_scale_mirror && c->v_scale_mirror;
+  return c->k_mirror && c->v_mirror;
+}
+
+bool mirror_consistent(const Dims& d, const ssa_cache* c) {
+  const bool any = c->k_mirror || c->v_mirror || c->k_scale_mirror || c->v_scale_mirror;
+  return !any || has_mirror(d, c);
+}
+
+int check_cache(const Dims& d, const ssa_cache* c) {
+  if (!c || !c->k_pool || !c->v_pool || !c->slab || !c->slot_of || !c->page_of || !c->last_use ||
+      !c->clock)
+    return SSA_ERR_INVALID_ARG;
+  if (d.fp8 && (!c->k_scale || !c->v_scale)) return SSA_ERR_INVALID_ARG;
+  if (!mirror_consistent(d, c)) return SSA_ERR_NO_MIRROR;
+  return SSA_OK;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 152;
+  }
+  return n;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace: [scores | miss_page | miss_slot | n_miss | part_o | part_ml],
+// each sized for the whole layer range of the layout.
+struct WsLayout {
+  size_t scores, miss_page, miss_slot, n_miss, part_o, part_ml, total;
+};
+
+size_t part_entries(const Dims& d) {
+  size_t best = 0;
+  for (int nl = 1; nl <= d.Lyr; ++nl) {
+    const size_t e = (size_t)nl * d.B * d.Hkv * decode_splits(d, nl, num_sms());
+    if (e > best) best = e;
+  }
+  return best * d.G;
+}
+
+WsLayout ws_layout(const Dims& d) {
+  WsLayout w{};
+  size_t off = 0;
+  w.scores = off;    off += align256((size_t)d.Lyr * d.B * d.nmax * 4);
+  w.miss_page = off; off += align256((size_t)d.Lyr * d.B * d.W * 4);
+  w.miss_slot = off; off += align256((size_t)d.Lyr * d.B * d.W * 4);
+  w.n_miss = off;    off += align256((size_t)d.Lyr * 4);
+  const size_t pe = part_entries(d);
+  w.part_o = off;    off += align256(pe * d.D * 4);
+  w.part_ml = off;   off += align256(pe * 2 * 4);
+  w.total = off;
+  return w;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+}  // namespace
+
+void count_launch(int n) { g_launches += n; }
+
+}  // namespace ssa
+
+using namespace ssa;
+
+extern "C" {
+
+size_t ssa_workspace_size(const ssa_layout* lay) {
+  Dims d;
+  if (check_layout(lay, d) != SSA_OK) return 0;
+  return ws_layout(d).total;
+}
+
+int ssa_lru_init(const ssa_layout* lay, const ssa_cache* c, int identity, ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if ((r = check_cache(d, c))) return r;
+  if (!c->slab_scale || !c->slab_sum || !c->slab_cnt) return SSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_lru_init(d, *c, identity ? 1 : 0, (cudaStream_t)stream);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
+int ssa_store_kv_mirror(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                        const void* k, const void* v, const int64_t* pos, int T,
+                        int32_t* status, ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if ((r = check_cache(d, c))) return r;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (T < 0 || (T > 0 && (!k || !v || !pos))) return SSA_ERR_INVALID_ARG;
+  if (!c->slab_scale || !c->slab_sum || !c->slab_cnt) return SSA_ERR_INVALID_ARG;
+  if (T > 2147483647 / 2) return SSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_store(d, *c, layer0, n_layers, k, v, pos, T, status,
+                               (cudaStream_t)stream);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
+int ssa_index_topk(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                   const void* q, const int32_t* block_table, const int32_t* seq_lens,
+                   int32_t* sel, int32_t* n_sel, int32_t* scores_opt, int32_t* status,
+                   void* ws, ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if (!c || !c->slab) return SSA_ERR_INVALID_ARG;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (!q || !block_table || !seq_lens || !sel || !n_sel) return SSA_ERR_INVALID_ARG;
+  if (!scores_opt && !ws) return SSA_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(d);
+  int32_t* scores = scores_opt ? scores_opt : at<int32_t>(ws, w.scores);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_index_scores(d, *c, layer0, n_layers, q, block_table, seq_lens, scores,
+                                      status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_topk_select(d, n_layers, scores, seq_lens, sel, n_sel, status, s);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
+int ssa_ensure_resident(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                        const int32_t* sel, const int32_t* block_table,
+                        int32_t* miss_page_opt, int32_t* miss_slot_opt, int32_t* n_miss_opt,
+                        int32_t* status, void* ws, ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if ((r = check_cache(d, c))) return r;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (!sel || !block_table) return SSA_ERR_INVALID_ARG;
+  const long long need = (long long)d.B * d.W < d.Lp ? (long long)d.B * d.W : d.Lp;
+  if (d.S < need) return SSA_ERR_POOL_TOO_SMALL;
+  if (!ws && (!miss_page_opt || !miss_slot_opt || !n_miss_opt)) return SSA_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(d);
+  int32_t* mp = miss_page_opt ? miss_page_opt : at<int32_t>(ws, w.miss_page);
+  int32_t* ms = miss_slot_opt ? miss_slot_opt : at<int32_t>(ws, w.miss_slot);
+  int32_t* nm = n_miss_opt ? n_miss_opt : at<int32_t>(ws, w.n_miss);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_ensure_state(d, *c, layer0, n_layers, sel, block_table, mp, ms, nm,
+                                      status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_miss_copy(d, *c, layer0, n_layers, mp, ms, nm, status, s);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
+int ssa_remap_block_table(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                          const int32_t* sel, const int32_t* block_table, int32_t* phys,
+                          int32_t* status, ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if (!c || !c->slot_of) return SSA_ERR_INVALID_ARG;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (!sel || !block_table || !phys) return SSA_ERR_INVALID_ARG;
+  cudaError_t e = launch_remap(d, *c, layer0, n_layers, sel, block_table, phys, status,
+                               (cudaStream_t)stream);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
+int ssa_sparse_paged_decode(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                            const void* q, const int32_t* sel, const int32_t* phys,
+                            const int32_t* seq_lens, float sm_scale, void* out,
+                            int32_t* status, void* ws, ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if (!c || !c->k_pool || !c->v_pool || (d.fp8 && (!c->k_scale || !c->v_scale)))
+    return SSA_ERR_INVALID_ARG;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (!q || !sel || !phys || !seq_lens || !out) return SSA_ERR_INVALID_ARG;
+  const int splits = decode_splits(d, n_layers, num_sms());
+  if (splits > 1 && !ws) return SSA_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(d);
+  DecodeArgs a{};
+  a.d = &d;
+  a.c = c;
+  a.layer0 = layer0;
+  a.n_layers = n_layers;
+  a.splits = splits;
+  a.q = q;
+  a.sel = sel;
+  a.phys = phys;
+  a.seq_lens = seq_lens;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.part_o = ws ? at<float>(ws, w.part_o) : nullptr;
+  a.part_ml = ws ? at<float>(ws, w.part_ml) : nullptr;
+  a.status = status;
+  cudaError_t e = launch_decode(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
+const char* ssa_status_str(int code) {
+  switch (code) {
+    case SSA_OK: return "ok";
+    case SSA_ERR_INVALID_ARG: return "invalid argument (null pointer, layer range or layout field)";
+    case SSA_ERR_POOL_TOO_SMALL: return "pool_slots < min(batch * max_sel, logical_pages)";
+    case SSA_ERR_UNSUPPORTED: return "unsupported layout (dtype, page size, head_dim, GQA group)";
+    case SSA_ERR_NO_MIRROR: return "host mirror pointers incomplete";
+    case SSA_ERR_CUDA: return "CUDA launch failed (see ssa_last_cuda_error)";
+    default: break;
+  }
+  if (code > 0) {
+    static thread_local char buf[256];
+    buf[0] = 0;
+    const char* names[] = {"drop", "bad_id", "miss_no_mirror", "unresolved", "bad_pos",
+                           "timeout"};
+    for (int i = 0; i < 6; ++i)
+      if (code & (1 << i)) {
+        if (buf[0]) strncat(buf, "|", sizeof(buf) - strlen(buf) - 1);
+        strncat(buf, names[i], sizeof(buf) - strlen(buf) - 1);
+      }
+    return buf;
+  }
+  return "unknown status";
+}
+
+int ssa_last_cuda_error(void) { return g_last_cuda_error; }
+
+long long ssa_launch_count(void) { return g_launches; }
+
+}  // extern "C"

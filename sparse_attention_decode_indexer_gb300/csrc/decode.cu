@@ -1,0 +1,586 @@
+// decode.cu -- a6 sparse paged GQA decode attention and a7 split merge.
+//
+// FreeToken PR #499, "Design": after ensure, the block table is translated
+// logical -> physical and the sparse paged attention runs on it, reading only
+// the selected pages.  For request b, KV head h and its G query heads:
+//     o[g] = sum_t softmax_t(sm_scale * q[g] . K[t]) V[t]
+// over the valid tokens of the selected pages (fp8: K = code * k_scale[t],
+// V = code * v_scale[t]).
+//
+// Design (sm_103a):
+//   * grid (split, b*Hkv+h, layer); each CTA takes a contiguous share of the
+//     valid selected pages of its (layer, request, KV head);
+//   * one producer warp streams each page's K and V (one KV head, P tokens)
+//     into shared memory with TMA tiled copies (128-byte swizzle), plus the
+//     fp8 per-token scales with bulk copies, through an mbarrier ring;
+//   * four consumer warps each take 16-token blocks: QK^T and PV as
+//     m16n8k16 tensor-core tiles with the G <= 8 query heads as the M rows,
+//     fp32 accumulate, online softmax in the log2 domain with warp shuffles;
+//   * bf16 K/V: bf16 MMAs, ldmatrix (V transposed by ldmatrix.trans);
+//   * fp8 K/V: the e4m3 codes convert exactly to f16, so the MMAs run in f16
+//     on the raw codes; q is scaled by a power of two into f16 range, the K
+//     scale multiplies the fp32 score, and the V scale folds into the
+//     probabilities (relative to a running power-of-two reference, so the
+//     f16 operand never overflows).  V is stored d-major in the pool
+//     ([Hkv][D][P]) so that the 8-bit reads run along tokens, the reduction
+//     axis of PV;
+//   * the 4 warps' states merge in shared memory; with several splits the
+//     CTA writes (m, l, o) partials and a merge kernel combines them.
+// The work is HBM-bound (8 flop/byte bf16, 16 fp8): the tensor cores carry
+// the G-row tiles, the memory system sets the pace.
+#include <cudaTypedefs.h>
+#include <cuda.h>
+#include <cmath>
+#include <cstdio>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ssa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kConsumerWarps = 4;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxG = 8;
+
+__host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+template <bool FP8, int P>
+struct Cfg {
+  static constexpr int kTileBytes = P * kD * (FP8 ? 1 : 2);      // one KV head of one page
+  static constexpr int kScaleBytes = FP8 ? 2 * P * 4 : 0;
+  static constexpr int kStageBytes = round_up(2 * kTileBytes + kScaleBytes, 1024);
+  static constexpr int kStages = FP8 ? 4 : 3;
+  static constexpr int kBlocks = P / 16;                          // 16-token blocks per page
+  // log2 of the fp8 V^T row swizzle span in 16-byte units (row = P bytes)
+  static constexpr int kVSwz = P >= 128 ? 3 : (P == 64 ? 2 : (P == 32 ? 1 : 0));
+  static_assert(kConsumerWarps * kMaxG * kD * 4 + 2 * kConsumerWarps * kMaxG * 4 <=
+                kStages * kStageBytes, "combine area must fit in the stage ring");
+};
+
+struct DecodeParams {
+  const __nv_bfloat16* q;   // [n_layers][B][Hq][D]
+  const int32_t* sel;       // [n_layers][B][W]
+  const int32_t* phys;
+  const int32_t* seq_lens;
+  const float* k_scale;     // [Lyr][S][P]
+  const float* v_scale;
+  __nv_bfloat16* out;       // [n_layers][B][Hq][D]
+  float* part_o;            // [units][splits][G][D]
+  float* part_ml;           // [units][splits][G][2]
+  int32_t* status;
+  int layer0, B, Hq, Hkv, G, W, S, splits;
+  float sm_log2;            // sm_scale * log2(e)
+};
+
+// byte offset inside a tile whose rows were written by TMA with a
+// 2^swz x 16-byte swizzle (bits [4, 4+swz) ^= bits [7, 7+swz))
+__device__ __forceinline__ uint32_t swz(uint32_t a, int bits) {
+  return a ^ (((a >> 7) & ((1u << bits) - 1u)) << 4);
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+template <bool FP8, int P>
+__global__ void __launch_bounds__(kDecodeThreads, FP8 ? 3 : 2)
+decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV) {
+  using C = Cfg<FP8, P>;
+  constexpr int NST = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  int2* plist = reinterpret_cast<int2*>(smem + NST * C::kStageBytes);     // [W]
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(plist + round_up(p.W, 2));  // [8][D]
+  uint64_t* full = reinterpret_cast<uint64_t*>(qs + kMaxG * kD);
+  uint64_t* empty = full + NST;
+  __shared__ int s_nv;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, bh = blockIdx.y, li = blockIdx.z;
+  const int b = bh / p.Hkv, h = bh - b * p.Hkv;
+  const int layer = p.layer0 + li;
+
+  if (tid == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  // valid selected pages of this (layer, request), in list order
+  if (warp == 0) {
+    const int32_t* selr = p.sel + ((size_t)li * p.B + b) * p.W;
+    const int32_t* physr = p.phys + ((size_t)li * p.B + b) * p.W;
+    int cnt = 0;
+    for (int base = 0; base < p.W; base += 32) {
+      const int i = base + lane;
+      int pg = -1, sl = -1;
+      if (i < p.W) { pg = selr[i]; sl = physr[i]; }
+      const bool ok = pg >= 0 && sl >= 0 && sl < p.S;
+      if (pg >= 0 && sl < 0) set_status(p.status, SSA_ST_UNRESOLVED);
+      if (pg >= 0 && sl >= p.S) set_status(p.status, SSA_ST_BAD_ID);
+      const unsigned m = __ballot_sync(0xffffffffu, ok);
+      if (ok) plist[cnt + __popc(m & ((1u << lane) - 1u))] = make_int2(pg, sl);
+      cnt += __popc(m);
+    }
+    if (lane == 0) s_nv = cnt;
+  }
+  // the G query rows of this KV head (rows >= G are zero)
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.q + (((size_t)li * p.B + b) * p.Hq + (size_t)h * p.G) * kD);
+    uint4* dst = reinterpret_cast<uint4*>(qs);
+    for (int i = tid; i < kMaxG * kD / 8; i += blockDim.x) {
+      const int g = i / (kD / 8);
+      dst[i] = g < p.G ? src[i] : make_uint4(0, 0, 0, 0);
+    }
+  }
+  __syncthreads();
+
+  const int nv = s_nv;
+  const int i0 = (int)((long long)nv * split / p.splits);
+  const int i1 = (int)((long long)nv * (split + 1) / p.splits);
+  const int nst = i1 - i0;
+  const int seq_len = p.seq_lens[b];
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: one elected thread issues every copy -------
+    if (lane != 0 || nst <= 0) return;
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    int issued = 0;
+    bool aborted = false;
+    for (int st = 0; st < nst; ++st) {
+      const int sb = st % NST;
+      if (st >= NST && !mbar_wait(&empty[sb], ((st / NST) - 1) & 1, &s_abort)) {
+        aborted = true;
+        break;
+      }
+      const int2 e = plist[i0 + st];
+      const int row_k = ((layer * p.S + e.y) * p.Hkv + h) * P;
+      uint8_t* stage = ring + sb * C::kStageBytes;
+      mbar_arrive_expect_tx(&full[sb], 2 * C::kTileBytes + C::kScaleBytes);
+      if (FP8) {
+        tma_load_2d(stage, &tmK, &full[sb], 0, row_k);
+        const int row_v = ((layer * p.S + e.y) * p.Hkv + h) * kD;
+        tma_load_2d(stage + C::kTileBytes, &tmV, &full[sb], 0, row_v);
+        const size_t so = ((size_t)layer * p.S + e.y) * P;
+        bulk_load(stage + 2 * C::kTileBytes, p.k_scale + so, P * 4, &full[sb]);
+        bulk_load(stage + 2 * C::kTileBytes + P * 4, p.v_scale + so, P * 4, &full[sb]);
+      } else {
+        tma_load_2d(stage, &tmK, &full[sb], 0, row_k);
+        tma_load_2d(stage + P * 128, &tmK, &full[sb], 64, row_k);
+        tma_load_2d(stage + C::kTileBytes, &tmV, &full[sb], 0, row_k);
+        tma_load_2d(stage + C::kTileBytes + P * 128, &tmV, &full[sb], 64, row_k);
+      }
+      ++issued;
+    }
+    if (aborted) {
+      s_abort = 1;
+      set_status(p.status, SSA_ST_TIMEOUT);
+      // let every copy still in flight land before the CTA can exit
+      for (int st = issued > NST ? issued - NST : 0; st < issued; ++st)
+        mbar_wait(&full[st % NST], (st / NST) & 1, nullptr);
+    }
+    return;
+  }
+
+  // ---------------- consumers -------------------------------------------------
+  const int g = lane >> 2, c = lane & 3;
+
+  // q fragments (A operand, rows = query heads); fp8 path: scaled to f16 range
+  uint32_t qa[8][2];
+  float qscale_log2 = p.sm_log2;
+  if (FP8) {
+    float amax = 0.0f;
+    for (int i = lane; i < kMaxG * kD; i += 32) amax = fmaxf(amax, fabsf(__bfloat162float(qs[i])));
+    amax = warp_max(amax);
+    int eq = 0;
+    if (amax > 0.0f) {
+      const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);     // amax in [2^(ef-127), 2^(ef-126))
+      eq = 141 - ef;                                                  // amax * 2^eq < 2^15
+      eq = eq > 126 ? 126 : (eq < -126 ? -126 : eq);
+    }
+    const float up = exp2f((float)eq);
+    qscale_log2 = p.sm_log2 * exp2f((float)-eq);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const __nv_bfloat16* r = qs + g * kD + 16 * ks + 4 * c;
+      qa[ks][0] = pack_f16(__bfloat162float(r[0]) * up, __bfloat162float(r[1]) * up);
+      qa[ks][1] = pack_f16(__bfloat162float(r[2]) * up, __bfloat162float(r[3]) * up);
+    }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qa[ks][0] = *reinterpret_cast<const uint32_t*>(qs + g * kD + 16 * ks + 2 * c);
+      qa[ks][1] = *reinterpret_cast<const uint32_t*>(qs + g * kD + 16 * ks + 2 * c + 8);
+    }
+  }
+
+  float o[16][4];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+  // fp8: probabilities carry v_scale / vref, vref a power of two above every
+  // V scale seen so far (0 until the first block sets it)
+  float m_run = -INFINITY, l_run = 0.0f, vref = FP8 ? 0.0f : 1.0f;
+
+  for (int st = 0; st < nst; ++st) {
+    const int sb = st % NST;
+    if (!mbar_wait(&full[sb], (st / NST) & 1, &s_abort)) {
+      s_abort = 1;
+      set_status(p.status, SSA_ST_TIMEOUT);
+      break;
+    }
+    const int2 e = plist[i0 + st];
+    const int nvalid = max(0, min(P, seq_len - e.x * P));
+    uint8_t* stage = ring + sb * C::kStageBytes;
+    const uint32_t kb = smem_u32(stage);
+    const uint32_t vb = kb + C::kTileBytes;
+    const float* ksc = reinterpret_cast<const float*>(stage + 2 * C::kTileBytes);
+    const float* vsc = ksc + P;
+
+#pragma unroll 1
+    for (int blk = 0; blk < C::kBlocks; ++blk) {
+      if (((st * C::kBlocks + blk) & (kConsumerWarps - 1)) != warp) continue;
+      const int tb = blk * 16;
+      // zero V of the tokens past seq_len (their bytes are not ours to trust)
+      if (nvalid < tb + 16) {
+        if (FP8) {
+          for (int i = lane; i < kD * 16; i += 32) {
+            const int d = i >> 4, x = tb + (i & 15);
+            if (x >= nvalid) stage[C::kTileBytes + swz(d * P + x, C::kVSwz)] = 0;
+          }
+        } else {
+          for (int i = lane; i < 16 * 16; i += 32) {
+            const int r = tb + (i >> 4), ch = i & 15;
+            if (r >= nvalid)
+              *reinterpret_cast<uint4*>(stage + C::kTileBytes + (ch >> 3) * (P * 128) + r * 128 +
+                                        (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+
+      // S = Q K^T for 16 tokens: two n8 tiles
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      int tok[4];   // token (within page) of s0[0], s0[1], s1[0], s1[1]
+      if (FP8) {
+        const int nB = lane >> 2, cB = nB >> 1, eB = nB & 1;
+        const int t0 = tb + 4 * cB + (cB < 2 ? eB : 2 + eB);
+        const int t1 = tb + 4 * cB + (cB < 2 ? 2 + eB : eB);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t w0 = lds32(kb + t0 * 128 + ((ks ^ (t0 & 7)) << 4) + 4 * c);
+          const uint32_t w1 = lds32(kb + t1 * 128 + ((ks ^ (t1 & 7)) << 4) + 4 * c);
+          mma_f16(s0, qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w0 >> 16));
+          mma_f16(s1, qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w1 >> 16));
+        }
+        tok[0] = tb + 4 * c + (c < 2 ? 0 : 2);
+        tok[1] = tok[0] + 1;
+        tok[2] = tb + 4 * c + (c < 2 ? 2 : 0);
+        tok[3] = tok[2] + 1;
+      } else {
+        const int mi = lane >> 3, r = lane & 7;
+        const int t = tb + (mi >> 1) * 8 + r;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const int chunk = 2 * ks + (mi & 1);
+          const uint32_t addr =
+              kb + (chunk >> 3) * (P * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(b0, b1, b2, b3, addr);
+          mma_bf16(s0, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+          mma_bf16(s1, qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+        }
+        tok[0] = tb + 2 * c;
+        tok[1] = tok[0] + 1;
+        tok[2] = tb + 8 + 2 * c;
+        tok[3] = tok[2] + 1;
+      }
+
+      // online softmax (log2 domain), rows g; lanes 4g..4g+3 share a row
+      float x[4] = {s0[0], s0[1], s1[0], s1[1]};
+      float vs[4];
+      float vmax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool valid = tok[i] < nvalid;
+        const float ksc_i = FP8 ? ksc[tok[i]] : 1.0f;
+        x[i] = valid ? x[i] * ksc_i * qscale_log2 : -INFINITY;
+        vs[i] = (FP8 && valid) ? vsc[tok[i]] : 0.0f;
+        vmax = fmaxf(vmax, vs[i]);
+      }
+      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+      float corr = exp2f(m_run - m_use);
+      float ocorr = corr;
+      if (FP8) {
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+        if (vmax >= vref) {
+          // next power of two above vmax; O rescales exactly
+          const float nref = __uint_as_float(((__float_as_uint(vmax) >> 23) + 1) << 23);
+          ocorr = corr * (vref / nref);
+          vref = nref;
+        }
+      }
+      float pr[4];
+      float lsum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float pi = exp2f(x[i] - m_use);
+        if (FP8) {
+          lsum += pi;
+          pr[i] = pi * (vs[i] / vref);
+        } else {
+          pr[i] = bf16_round(pi);
+          lsum += pr[i];
+        }
+      }
+      l_run = l_run * corr + lsum;
+      m_run = m_new;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) { o[n][0] *= ocorr; o[n][1] *= ocorr; }
+
+      // O += P V
+      if (FP8) {
+        const uint32_t a0 = pack_f16(pr[0], pr[1]), a2 = pack_f16(pr[2], pr[3]);
+        const int dn = lane >> 2;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          const int d = 8 * n + dn;
+          const uint32_t w = lds32(vb + swz(d * P + tb + 4 * c, C::kVSwz));
+          const uint32_t lo = e4m3x2_to_f16x2(w), hi = e4m3x2_to_f16x2(w >> 16);
+          mma_f16(o[n], a0, 0u, a2, 0u, c < 2 ? lo : hi, c < 2 ? hi : lo);
+        }
+      } else {
+        const uint32_t a0 = pack_bf16(pr[0], pr[1]), a2 = pack_bf16(pr[2], pr[3]);
+        const int mi = lane >> 3, r = lane & 7;
+        const int t = tb + (mi & 1) * 8 + r;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int chunk = 2 * j + (mi >> 1);
+          const uint32_t addr =
+              vb + (chunk >> 3) * (P * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_t(v0, v1, v2, v3, addr);
+          mma_bf16(o[2 * j], a0, 0u, a2, 0u, v0, v1);
+          mma_bf16(o[2 * j + 1], a0, 0u, a2, 0u, v2, v3);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[sb]);
+  }
+
+  // ---------------- merge the 4 warps' states (stage ring is idle now) ------
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  consumer_sync();
+  float* cO = reinterpret_cast<float*>(ring);                  // [4][8][D]
+  float* cM = cO + kConsumerWarps * kMaxG * kD;                 // [4][8]
+  float* cL = cM + kConsumerWarps * kMaxG;                      // [4][8]
+#pragma unroll
+  for (int n = 0; n < 16; ++n) {
+    const int d = 8 * n + 2 * c;
+    cO[(warp * kMaxG + g) * kD + d] = o[n][0] * vref;
+    cO[(warp * kMaxG + g) * kD + d + 1] = o[n][1] * vref;
+  }
+  if (c == 0) {
+    cM[warp * kMaxG + g] = m_run;
+    cL[warp * kMaxG + g] = l_run;
+  }
+  consumer_sync();
+  const int unit = (li * p.B + b) * p.Hkv + h;
+  for (int i = tid; i < kMaxG * kD; i += kConsumerWarps * 32) {
+    const int gg = i / kD, d = i - gg * kD;
+    if (gg >= p.G) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cM[w * kMaxG + gg]);
+    float L = 0.0f, O = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float f = exp2f(cM[w * kMaxG + gg] - M);
+        L += cL[w * kMaxG + gg] * f;
+        O += cO[(w * kMaxG + gg) * kD + d] * f;
+      }
+    }
+    if (p.splits == 1) {
+      const float r = L > 0.0f ? O / L : 0.0f;
+      p.out[(((size_t)li * p.B + b) * p.Hq + h * p.G + gg) * kD + d] = __float2bfloat16_rn(r);
+    } else {
+      const size_t pi = ((size_t)unit * p.splits + split) * p.G + gg;
+      p.part_o[pi * kD + d] = O;
+      if (d == 0) {
+        p.part_ml[pi * 2] = M;
+        p.part_ml[pi * 2 + 1] = L;
+      }
+    }
+  }
+}
+
+// a7: combine the splits' (m, l, o) partials of one (layer, request, KV head)
+__global__ void __launch_bounds__(256)
+merge_kernel(const float* part_o, const float* part_ml, __nv_bfloat16* out, int splits,
+             int B, int Hq, int Hkv, int G) {
+  const int unit = blockIdx.x;
+  const int h = unit % Hkv, lb = unit / Hkv;            // lb = li * B + b
+  for (int i = threadIdx.x; i < G * kD; i += blockDim.x) {
+    const int g = i / kD, d = i - g * kD;
+    float M = -INFINITY;
+    for (int s = 0; s < splits; ++s)
+      M = fmaxf(M, part_ml[(((size_t)unit * splits + s) * G + g) * 2]);
+    float L = 0.0f, O = 0.0f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < splits; ++s) {
+        const size_t pi = ((size_t)unit * splits + s) * G + g;
+        const float f = exp2f(part_ml[pi * 2] - M);
+        L += part_ml[pi * 2 + 1] * f;
+        O += part_o[pi * kD + d] * f;
+      }
+    }
+    out[((size_t)lb * Hq + h * G + g) * kD + d] = __float2bfloat16_rn(L > 0.0f ? O / L : 0.0f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool make_tmap(CUtensorMap* tm, void* base, CUtensorMapDataType dt, int esz, uint64_t inner,
+               uint64_t rows, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * (uint64_t)esz};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool FP8, int P>
+size_t decode_smem(int W) {
+  using C = Cfg<FP8, P>;
+  return 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)round_up(W, 2) * 8 +
+         kMaxG * kD * 2 + 2 * C::kStages * 8;
+}
+
+template <bool FP8, int P>
+cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeParams& p, cudaStream_t s) {
+  const Dims& d = *a.d;
+  const ssa_cache& c = *a.c;
+  CUtensorMap tmK, tmV;
+  const uint64_t rows_tok = (uint64_t)d.Lyr * d.S * d.Hkv * P;
+  bool ok;
+  if (FP8) {
+    ok = make_tmap(&tmK, c.k_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kD, rows_tok, kD, P,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    const CUtensorMapSwizzle vsw = P >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : P == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : P == 32  ? CU_TENSOR_MAP_SWIZZLE_32B
+                                            : CU_TENSOR_MAP_SWIZZLE_NONE;
+    ok = ok && make_tmap(&tmV, c.v_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, P,
+                         (uint64_t)d.Lyr * d.S * d.Hkv * kD, P, kD, vsw);
+  } else {
+    ok = make_tmap(&tmK, c.k_pool, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, rows_tok, 64, P,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_tmap(&tmV, c.v_pool, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, rows_tok, 64, P,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  const size_t smem = decode_smem<FP8, P>(d.W);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP8, P>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.splits, d.B * d.Hkv, a.n_layers);
+  decode_kernel<FP8, P><<<grid, kDecodeThreads, smem, s>>>(p, tmK, tmV);
+  count_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.splits == 1) return e;
+  merge_kernel<<<a.n_layers * d.B * d.Hkv, 256, 0, s>>>(
+      a.part_o, a.part_ml, static_cast<__nv_bfloat16*>(a.out), a.splits, d.B, d.Hq, d.Hkv, d.G);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_splits(const Dims& d, int n_layers, int num_sms) {
+  const long long units = (long long)n_layers * d.B * d.Hkv;
+  const int ctas_per_sm = d.fp8 ? 3 : 2;
+  const long long target = (long long)num_sms * ctas_per_sm;
+  long long s = (target + units - 1) / units;
+  const int max_s = d.max_selected() / 2 > 1 ? d.max_selected() / 2 : 1;
+  if (s > max_s) s = max_s;
+  if (s < 1) s = 1;
+  return (int)s;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  const Dims& d = *a.d;
+  const ssa_cache& c = *a.c;
+  DecodeParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.sel = a.sel;
+  p.phys = a.phys;
+  p.seq_lens = a.seq_lens;
+  p.k_scale = c.k_scale;
+  p.v_scale = c.v_scale;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.part_o = a.part_o;
+  p.part_ml = a.part_ml;
+  p.status = a.status;
+  p.layer0 = a.layer0;
+  p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.G = d.G; p.W = d.W; p.S = d.S;
+  p.splits = a.splits;
+  p.sm_log2 = a.sm_scale * 1.4426950408889634f;
+  switch (d.P * 2 + d.fp8) {
+    case 32: return launch_decode_t<false, 16>(a, p, s);
+    case 33: return launch_decode_t<true, 16>(a, p, s);
+    case 64: return launch_decode_t<false, 32>(a, p, s);
+    case 65: return launch_decode_t<true, 32>(a, p, s);
+    case 128: return launch_decode_t<false, 64>(a, p, s);
+    case 129: return launch_decode_t<true, 64>(a, p, s);
+    case 256: return launch_decode_t<false, 128>(a, p, s);
+    case 257: return launch_decode_t<true, 128>(a, p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ssa

@@ -1,0 +1,367 @@
+// ensure.cu -- a3 LRU ensure, a4 miss fetch, a5 block-table remap.
+//
+// FreeToken PR #499, "What": the GPU pool is an LRU cache of physical slots
+// over the logical page space, backed by the pinned host mirror.  "Design":
+// lru_ensure is a device-side LRU with fixed shapes (graph-safe, no host
+// sync, no data-dependent shapes); eviction is a pure rebind because slots
+// are drop-clean; fast_index_copy moves K+V of each miss host -> device.
+// FreeToken PR #525: the copy carries the per-token scale banks, and the
+// whole batch selection fits the pool by construction.
+//
+// Order of events per layer (the pages state none; this is the reading the
+// library takes, identical in the oracle):
+//   1. U = distinct selected logical ids, ascending (bitonic sort + dedup);
+//   2. hits: last_use = clock;
+//   3. misses, ascending, take victims in order: free slots by slot id, then
+//      bound slots not touched this step by (last_use, slot) -- the m
+//      smallest keys found by an MSB radix select, then sorted;
+//   4. rebind; 5. clock += 1.
+// One CTA per layer: the state update is latency-bound (a few thousand keys),
+// the copy that follows is a separate, wide kernel.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ssa {
+namespace {
+
+constexpr int kEnsureThreads = 1024;
+
+template <typename T>
+__device__ void bitonic_sort_smem(T* a, int n /* power of two */) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool up = (i & k) == 0;
+          const T x = a[i], y = a[ixj];
+          if ((x > y) == up) { a[i] = y; a[ixj] = x; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+struct EnsureParams {
+  int32_t *slot_of, *page_of, *last_use, *clock;
+  const int32_t* sel;    // [n_layers][B][W]
+  const int32_t* bt;     // [B][nmax]
+  int32_t* miss_page;    // [n_layers][B*W]
+  int32_t* miss_slot;
+  int32_t* n_miss;       // [n_layers]
+  int32_t* status;
+  int layer0, Lp, S, B, W, nmax, N2;
+  int has_mirror;
+};
+
+__device__ __forceinline__ uint32_t victim_key(const int32_t* page_of, const int32_t* last_use,
+                                               int s, int32_t clock) {
+  const int32_t po = page_of[s], lu = last_use[s];
+  if (po >= 0 && lu == clock) return 0xFFFFFFFFu;             // touched this step: a hit
+  const int32_t k = po < 0 ? -2 : lu;                          // free slots first
+  return (uint32_t)k ^ 0x80000000u;
+}
+
+__global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsureParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const int N2 = p.N2;
+  uint64_t* vic = reinterpret_cast<uint64_t*>(smem_raw);            // [N2]
+  uint32_t* ids = reinterpret_cast<uint32_t*>(smem_raw + (size_t)N2 * 8);  // [N2]
+  __shared__ int hist[256];
+  __shared__ int tmp[33];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining, s_nv;
+
+  const int li = blockIdx.x, layer = p.layer0 + li;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int BW = p.B * p.W;
+  int32_t* slot_of = p.slot_of + (size_t)layer * p.Lp;
+  int32_t* page_of = p.page_of + (size_t)layer * p.S;
+  int32_t* last_use = p.last_use + (size_t)layer * p.S;
+  int32_t* mpage = p.miss_page + (size_t)li * BW;
+  int32_t* mslot = p.miss_slot + (size_t)li * BW;
+  const int32_t clock = p.clock[layer];
+
+  // 1. gather selected logical ids, sort, dedup
+  for (int i = tid; i < N2; i += nt) {
+    uint32_t key = 0xFFFFFFFFu;
+    if (i < BW) {
+      const int b = i / p.W;
+      const int pg = p.sel[((size_t)li * p.B + b) * p.W + (i - b * p.W)];
+      if (pg >= 0) {
+        const int id = pg < p.nmax ? p.bt[(size_t)b * p.nmax + pg] : -1;
+        if (id >= 0 && id < p.Lp) key = (uint32_t)id;
+        else set_status(p.status, SSA_ST_BAD_ID);
+      }
+    }
+    ids[i] = key;
+  }
+  __syncthreads();
+  bitonic_sort_smem(ids, N2);
+
+  // 2. hits are touched; misses ranked in ascending id order
+  const int per = (N2 + nt - 1) / nt;
+  const int a0 = min(N2, tid * per), a1 = min(N2, a0 + per);
+  int my_miss = 0;
+  for (int i = a0; i < a1; ++i) {
+    const uint32_t id = ids[i];
+    if (id == 0xFFFFFFFFu || (i > 0 && ids[i - 1] == id)) continue;
+    const int slot = slot_of[id];
+    if (slot >= p.S) { set_status(p.status, SSA_ST_BAD_ID); continue; }   // corrupt state
+    if (slot >= 0) last_use[slot] = clock;
+    else ++my_miss;
+  }
+  int m;
+  int rank = block_exclusive_scan(my_miss, tmp, m);
+  for (int i = a0; i < a1; ++i) {
+    const uint32_t id = ids[i];
+    if (id == 0xFFFFFFFFu || (i > 0 && ids[i - 1] == id)) continue;
+    if (slot_of[id] < 0) mpage[rank++] = (int32_t)id;
+  }
+  __syncthreads();   // last_use touches and the miss list are visible block-wide
+
+  if (m > 0) {
+    // 3. the m smallest victim keys: MSB-first radix select on 32-bit keys
+    if (tid == 0) { s_prefix = 0; s_remaining = m; s_nv = 0; }
+    uint32_t mask = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += nt) hist[i] = 0;
+      __syncthreads();
+      const uint32_t prefix = s_prefix;
+      for (int s = tid; s < p.S; s += nt) {
+        const uint32_t kk = victim_key(page_of, last_use, s, clock);
+        if ((kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255], 1);
+      }
+      __syncthreads();
+      if (tid < 32) {
+        int cnt[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { cnt[j] = hist[8 * tid + j]; sum += cnt[j]; }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (tid >= o) incl += y;
+        }
+        const int rem = s_remaining;
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= rem);
+        const int lane = __ffs(hit) - 1;
+        if (tid == lane) {
+          int below = incl - sum;
+          for (int j = 0; j < 8; ++j) {
+            if (below + cnt[j] >= rem) {
+              s_remaining = rem - below;
+              s_prefix = prefix | ((uint32_t)(8 * tid + j) << shift);
+              break;
+            }
+            below += cnt[j];
+          }
+        }
+      }
+      mask |= 0xFFu << shift;
+      __syncthreads();
+    }
+    const uint32_t T = s_prefix;
+    const int need_eq = s_remaining;
+    // gather: keys below T (any order), then the need_eq lowest slots equal to T
+    const int sper = (p.S + nt - 1) / nt;
+    const int s0 = min(p.S, tid * sper), s1 = min(p.S, s0 + sper);
+    int eq = 0;
+    for (int s = s0; s < s1; ++s) {
+      const uint32_t kk = victim_key(page_of, last_use, s, clock);
+      if (kk < T) vic[atomicAdd(&s_nv, 1)] = ((uint64_t)kk << 32) | (uint32_t)s;
+      else if (kk == T) ++eq;
+    }
+    int eqtot;
+    int er = block_exclusive_scan(eq, tmp, eqtot);
+    const int n_lt = m - need_eq;
+    for (int s = s0; s < s1 && er < need_eq; ++s) {
+      const uint32_t kk = victim_key(page_of, last_use, s, clock);
+      if (kk == T) {
+        if (er < need_eq) vic[n_lt + er] = ((uint64_t)kk << 32) | (uint32_t)s;
+        ++er;
+      }
+    }
+    int M2 = 1;
+    while (M2 < m) M2 <<= 1;
+    for (int i = m + tid; i < M2; i += nt) vic[i] = ~0ull;
+    __syncthreads();
+    bitonic_sort_smem(vic, M2);
+
+    // 4. rebind: i-th miss takes the i-th victim
+    for (int i = tid; i < m; i += nt) {
+      const int pg = mpage[i];
+      const int v = (int)(uint32_t)(vic[i] & 0xFFFFFFFFu);
+      const int old = page_of[v];
+      if (old >= 0 && old < p.Lp) slot_of[old] = -1;
+      slot_of[pg] = v;
+      page_of[v] = pg;
+      last_use[v] = clock;
+      mslot[i] = v;
+    }
+    if (tid == 0 && !p.has_mirror) set_status(p.status, SSA_ST_MISS_NO_MIRROR);
+  }
+  for (int i = m + tid; i < BW; i += nt) { mpage[i] = -1; mslot[i] = -1; }
+  __syncthreads();
+  if (tid == 0) {
+    p.n_miss[li] = m;
+    p.clock[layer] = clock + 1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a4: copy each miss's page (K, V, fp8 scales) mirror -> slot.  Fixed grid of
+// B*W entries per layer; entries past the device-side miss count return.
+// 16-byte loads from pinned host memory over UVA, several in flight per
+// thread, 16-byte stores to HBM.
+// ---------------------------------------------------------------------------
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+constexpr int kCopyChunk = kCopyThreads * kCopyUnroll;   // 16-byte units per CTA
+
+struct CopyParams {
+  const uint8_t *k_mir, *v_mir;
+  const float *ks_mir, *vs_mir;
+  uint8_t *k_pool, *v_pool;
+  float *k_scale, *v_scale;
+  const int32_t *miss_page, *miss_slot, *n_miss;
+  int layer0, Lp, S, BW, P, fp8;
+  long long page_bytes;   // one page, all KV heads
+};
+
+__global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(CopyParams p) {
+  const int entry = blockIdx.y, li = blockIdx.z, layer = p.layer0 + li;
+  if (entry >= p.n_miss[li] || p.k_mir == nullptr) return;
+  const int pg = p.miss_page[(size_t)li * p.BW + entry];
+  const int slot = p.miss_slot[(size_t)li * p.BW + entry];
+  if (pg < 0 || pg >= p.Lp || slot < 0 || slot >= p.S) return;
+  const long long pb16 = p.page_bytes / 16;
+  const long long sc16 = p.fp8 ? (long long)p.P * 4 / 16 : 0;
+  const long long total = 2 * pb16 + 2 * sc16;
+  const size_t mp = (size_t)layer * p.Lp + pg, ps = (size_t)layer * p.S + slot;
+  // 16-byte unit idx of the concatenation [K page | V page | K scales | V scales]
+  auto locate = [&](long long idx, const uint4*& src, uint4*& dst) {
+    if (idx < pb16) {
+      src = reinterpret_cast<const uint4*>(p.k_mir + mp * p.page_bytes) + idx;
+      dst = reinterpret_cast<uint4*>(p.k_pool + ps * p.page_bytes) + idx;
+    } else if (idx < 2 * pb16) {
+      idx -= pb16;
+      src = reinterpret_cast<const uint4*>(p.v_mir + mp * p.page_bytes) + idx;
+      dst = reinterpret_cast<uint4*>(p.v_pool + ps * p.page_bytes) + idx;
+    } else if (idx < 2 * pb16 + sc16) {
+      idx -= 2 * pb16;
+      src = reinterpret_cast<const uint4*>(p.ks_mir + mp * p.P) + idx;
+      dst = reinterpret_cast<uint4*>(p.k_scale + ps * p.P) + idx;
+    } else {
+      idx -= 2 * pb16 + sc16;
+      src = reinterpret_cast<const uint4*>(p.vs_mir + mp * p.P) + idx;
+      dst = reinterpret_cast<uint4*>(p.v_scale + ps * p.P) + idx;
+    }
+  };
+  uint4 buf[kCopyUnroll];
+  uint4* dst[kCopyUnroll];
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u) {
+    const long long idx = (long long)blockIdx.x * kCopyChunk + u * kCopyThreads + threadIdx.x;
+    dst[u] = nullptr;
+    if (idx < total) {
+      const uint4* src;
+      locate(idx, src, dst[u]);
+      buf[u] = *src;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u)
+    if (dst[u]) *dst[u] = buf[u];
+}
+
+// ---------------------------------------------------------------------------
+// a5: phys[b][i] = slot_of[bt[b][sel[b][i]]], -1 for padding.
+// ---------------------------------------------------------------------------
+__global__ void remap_kernel(const int32_t* slot_of, const int32_t* sel, const int32_t* bt,
+                             int32_t* phys, int32_t* status, int layer0, int n_layers, int Lp,
+                             int B, int W, int nmax) {
+  const long long n = (long long)n_layers * B * W;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int li = (int)(i / ((long long)B * W));
+    const int b = (int)((i / W) % B);
+    const int pg = sel[i];
+    int out = -1;
+    if (pg >= 0) {
+      const int id = pg < nmax ? bt[(size_t)b * nmax + pg] : -1;
+      if (id >= 0 && id < Lp) out = slot_of[(size_t)(layer0 + li) * Lp + id];
+      else set_status(status, SSA_ST_BAD_ID);
+      if (out < 0) set_status(status, SSA_ST_UNRESOLVED);
+    }
+    phys[i] = out;
+  }
+}
+
+}  // namespace
+
+int ensure_sort_width(const Dims& d) {
+  int n = 2;
+  while (n < d.B * d.W) n <<= 1;
+  return n;
+}
+
+cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                                const int32_t* sel, const int32_t* bt, int32_t* miss_page,
+                                int32_t* miss_slot, int32_t* n_miss, int32_t* status,
+                                cudaStream_t s) {
+  EnsureParams p{};
+  p.slot_of = c.slot_of; p.page_of = c.page_of; p.last_use = c.last_use; p.clock = c.clock;
+  p.sel = sel; p.bt = bt; p.miss_page = miss_page; p.miss_slot = miss_slot; p.n_miss = n_miss;
+  p.status = status;
+  p.layer0 = layer0; p.Lp = d.Lp; p.S = d.S; p.B = d.B; p.W = d.W; p.nmax = d.nmax;
+  p.N2 = ensure_sort_width(d);
+  p.has_mirror = c.k_mirror != nullptr;
+  const size_t smem = (size_t)p.N2 * 12;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(ensure_state_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  ensure_state_kernel<<<n_layers, kEnsureThreads, smem, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                             const int32_t* miss_page, const int32_t* miss_slot,
+                             const int32_t* n_miss, int32_t* status, cudaStream_t s) {
+  (void)status;
+  if (c.k_mirror == nullptr) return cudaSuccess;   // nothing to fetch from (flagged by ensure)
+  CopyParams p{};
+  p.k_mir = static_cast<const uint8_t*>(c.k_mirror);
+  p.v_mir = static_cast<const uint8_t*>(c.v_mirror);
+  p.ks_mir = c.k_scale_mirror; p.vs_mir = c.v_scale_mirror;
+  p.k_pool = static_cast<uint8_t*>(c.k_pool); p.v_pool = static_cast<uint8_t*>(c.v_pool);
+  p.k_scale = c.k_scale; p.v_scale = c.v_scale;
+  p.miss_page = miss_page; p.miss_slot = miss_slot; p.n_miss = n_miss;
+  p.layer0 = layer0; p.Lp = d.Lp; p.S = d.S; p.BW = d.B * d.W; p.P = d.P; p.fp8 = d.fp8;
+  p.page_bytes = (long long)d.page_bytes();
+  const long long total16 = 2 * p.page_bytes / 16 + (d.fp8 ? 2LL * d.P * 4 / 16 : 0);
+  dim3 grid((unsigned)((total16 + kCopyChunk - 1) / kCopyChunk), p.BW, n_layers);
+  miss_copy_kernel<<<grid, kCopyThreads, 0, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_remap(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                         const int32_t* sel, const int32_t* bt, int32_t* phys,
+                         int32_t* status, cudaStream_t s) {
+  const long long n = (long long)n_layers * d.B * d.W;
+  const int threads = 256;
+  const int blocks = (int)((n + threads - 1) / threads);
+  remap_kernel<<<blocks, threads, 0, s>>>(c.slot_of, sel, bt, phys, status, layer0, n_layers,
+                                          d.Lp, d.B, d.W, d.nmax);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace ssa

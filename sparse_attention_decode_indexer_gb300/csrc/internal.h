@@ -1,0 +1,73 @@
+// internal.h -- launchers that the C ABI (api.cu) calls; one translation unit
+// per stage of the decode step.  Host-side only; no torch types anywhere.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ssa.h"
+
+namespace ssa {
+
+// Validated, derived view of an ssa_layout.
+struct Dims {
+  int P, Hq, Hkv, D, G, fp8, Lyr, Lp, S, B, nmax, k, W;
+  size_t esz() const { return fp8 ? 1 : 2; }
+  // bytes of one KV head of one page (K or V), and of a whole page (all heads)
+  size_t head_page_bytes() const { return (size_t)P * D * esz(); }
+  size_t page_bytes() const { return (size_t)Hkv * head_page_bytes(); }
+  int max_selected() const { return k + 1 < nmax ? k + 1 : nmax; }
+};
+
+// Split count of the attention kernel for a layer range (host heuristic);
+// the workspace holds partials for any count this returns.
+int decode_splits(const Dims& d, int n_layers, int num_sms);
+
+// -- store.cu ---------------------------------------------------------------
+cudaError_t launch_lru_init(const Dims& d, const ssa_cache& c, int identity, cudaStream_t s);
+cudaError_t launch_store(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                         const void* k, const void* v, const int64_t* pos, int T,
+                         int32_t* status, cudaStream_t s);
+
+// -- index.cu ---------------------------------------------------------------
+cudaError_t launch_index_scores(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                                const void* q, const int32_t* bt, const int32_t* seq_lens,
+                                int32_t* scores, int32_t* status, cudaStream_t s);
+cudaError_t launch_topk_select(const Dims& d, int n_layers, const int32_t* scores,
+                               const int32_t* seq_lens, int32_t* sel, int32_t* n_sel,
+                               int32_t* status, cudaStream_t s);
+
+// -- ensure.cu --------------------------------------------------------------
+cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                                const int32_t* sel, const int32_t* bt, int32_t* miss_page,
+                                int32_t* miss_slot, int32_t* n_miss, int32_t* status,
+                                cudaStream_t s);
+cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                             const int32_t* miss_page, const int32_t* miss_slot,
+                             const int32_t* n_miss, int32_t* status, cudaStream_t s);
+cudaError_t launch_remap(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                         const int32_t* sel, const int32_t* bt, int32_t* phys,
+                         int32_t* status, cudaStream_t s);
+
+// -- decode.cu --------------------------------------------------------------
+struct DecodeArgs {
+  const Dims* d;
+  const ssa_cache* c;
+  int layer0, n_layers, splits;
+  const void* q;
+  const int32_t* sel;
+  const int32_t* phys;
+  const int32_t* seq_lens;
+  float sm_scale;
+  void* out;
+  float* part_o;   // [units][splits][G][D]
+  float* part_ml;  // [units][splits][G][2]
+  int32_t* status;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// Counts every kernel launch the library enqueues (per host thread).
+void count_launch(int n = 1);
+
+}  // namespace ssa

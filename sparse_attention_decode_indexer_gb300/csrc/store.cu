@@ -1,0 +1,263 @@
+// store.cu -- a0: store K/V through the write-through host mirror, update the
+// indexer slab; and the residency-state reset.
+//
+// FreeToken PR #499, "Design": every store is mirrored to a pinned host bank
+// over UVA, so a GPU slot is always drop-clean and eviction is a pure rebind.
+// FreeToken PR #525 (mirror_store_quant): for an fp8 pool the mirror receives
+// the e4m3 codes and fp32 scales AFTER quantisation -- the pool is the source
+// of truth and the two hold identical bytes.
+//
+// One CTA per run of consecutive tokens of one logical page (the CTA of the
+// run's first token does the work; every other CTA returns at once), so the
+// slab's running sums are accumulated in token order by a single thread per
+// element and the result is independent of scheduling.  Rounding: IEEE fp32
+// division and rintf, e4m3 round-to-nearest-even with saturation -- the same
+// operations the definition states, one at a time.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ssa {
+namespace {
+
+struct StoreParams {
+  uint8_t *k_pool, *v_pool;
+  float *k_scale, *v_scale;
+  uint8_t *k_mir, *v_mir;
+  float *k_scale_m, *v_scale_m;
+  int8_t* slab;
+  float* slab_scale;
+  float* slab_sum;
+  int32_t* slab_cnt;
+  const int32_t* slot_of;
+  const __nv_bfloat16 *k, *v;   // [n_layers][T][HD]
+  const int64_t* pos;
+  int T;
+  int32_t* status;
+  int layer0, Lp, S, Hkv, D, P, fp8;
+};
+
+constexpr int kMaxPage = 128;
+
+__device__ __forceinline__ uint8_t e4m3(float x) {
+  return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+__global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
+  extern __shared__ uint8_t vt[];          // fp8 V of a full page, [HD][P]
+  __shared__ float s_ks[kMaxPage], s_vs[kMaxPage];
+  __shared__ int s_j[kMaxPage];
+  __shared__ int s_run;
+  __shared__ float red[33];
+  const int t0 = blockIdx.x, li = blockIdx.y, layer = p.layer0 + li;
+  const int tid = threadIdx.x, P = p.P, HD = p.Hkv * p.D;
+
+  const int64_t pos0 = p.pos[t0];
+  if (pos0 < 0 || pos0 / P >= p.Lp) {
+    if (tid == 0) set_status(p.status, SSA_ST_BAD_ID);
+    return;
+  }
+  const int pg = (int)(pos0 / P);
+  if (t0 > 0) {
+    const int64_t prev = p.pos[t0 - 1];
+    if (prev >= pos0 && tid == 0) set_status(p.status, SSA_ST_BAD_POS);
+    if (prev >= 0 && prev / P == pg) return;          // not the first token of its run
+  }
+  // run length: consecutive tokens of the same page (at most P)
+  if (tid == 0) s_run = P;
+  __syncthreads();
+  if (tid >= 1 && tid < P) {
+    const int t = t0 + tid;
+    bool ends = t >= p.T;
+    if (!ends) {
+      const int64_t x = p.pos[t];
+      ends = x < 0 || x / P != pg;
+      if (!ends && x <= p.pos[t - 1]) set_status(p.status, SSA_ST_BAD_POS);
+    }
+    if (ends) atomicMin(&s_run, tid);
+  }
+  __syncthreads();
+  const int R = s_run;
+  if (tid < R) s_j[tid] = (int)(p.pos[t0 + tid] % P);
+  __syncthreads();
+
+  int slot = p.slot_of[(size_t)layer * p.Lp + pg];
+  if (slot >= p.S) {                                    // corrupt state: never write through it
+    if (tid == 0) set_status(p.status, SSA_ST_BAD_ID);
+    slot = -1;
+  }
+  const size_t esz = p.fp8 ? 1 : 2;
+  const size_t pe = (size_t)HD * P;                    // elements per page block
+  uint8_t* km = p.k_mir ? p.k_mir + ((size_t)layer * p.Lp + pg) * pe * esz : nullptr;
+  uint8_t* vm = p.v_mir ? p.v_mir + ((size_t)layer * p.Lp + pg) * pe * esz : nullptr;
+  uint8_t* kp = slot >= 0 ? p.k_pool + ((size_t)layer * p.S + slot) * pe * esz : nullptr;
+  uint8_t* vp = slot >= 0 ? p.v_pool + ((size_t)layer * p.S + slot) * pe * esz : nullptr;
+  const __nv_bfloat16* kin = p.k + ((size_t)li * p.T + t0) * HD;
+  const __nv_bfloat16* vin = p.v + ((size_t)li * p.T + t0) * HD;
+
+  // phase 1 (fp8): per-token scales, one warp per token
+  if (p.fp8) {
+    const int lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    for (int r = warp; r < R; r += nw) {
+      float ak = 0.0f, av = 0.0f;
+      for (int e = lane; e < HD; e += 32) {
+        ak = fmaxf(ak, fabsf(__bfloat162float(kin[(size_t)r * HD + e])));
+        av = fmaxf(av, fabsf(__bfloat162float(vin[(size_t)r * HD + e])));
+      }
+      ak = warp_max(ak);
+      av = warp_max(av);
+      if (lane == 0) {
+        const float sk = ak > 0.0f ? ak / 448.0f : 1.0f;
+        const float sv = av > 0.0f ? av / 448.0f : 1.0f;
+        s_ks[r] = sk;
+        s_vs[r] = sv;
+        const size_t so_m = ((size_t)layer * p.Lp + pg) * P + s_j[r];
+        if (p.k_scale_m) { p.k_scale_m[so_m] = sk; p.v_scale_m[so_m] = sv; }
+        if (slot >= 0) {
+          const size_t so_p = ((size_t)layer * p.S + slot) * P + s_j[r];
+          p.k_scale[so_p] = sk;
+          p.v_scale[so_p] = sv;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // phase 2: codes, mirror + pool writes, slab running sum (token order)
+  const bool full_page = (R == P);
+  for (int e = tid; e < HD; e += blockDim.x) {
+    const int h = e / p.D, d = e - h * p.D;
+    float sum = p.slab_sum[((size_t)layer * p.Lp + pg) * HD + e];
+    for (int r = 0; r < R; ++r) {
+      const int j = s_j[r];
+      const __nv_bfloat16 xk = kin[(size_t)r * HD + e];
+      const __nv_bfloat16 xv = vin[(size_t)r * HD + e];
+      const size_t off = ((size_t)h * P + j) * p.D + d;             // [h][j][d]
+      if (p.fp8) {
+        const uint8_t ck = e4m3(__bfloat162float(xk) / s_ks[r]);
+        const uint8_t cv = e4m3(__bfloat162float(xv) / s_vs[r]);
+        const size_t offt = ((size_t)h * p.D + d) * P + j;          // V: [h][d][j]
+        if (km) km[off] = ck;
+        if (kp) kp[off] = ck;
+        if (full_page) {
+          vt[(size_t)e * P + j] = cv;
+        } else {
+          if (vm) vm[offt] = cv;
+          if (vp) vp[offt] = cv;
+        }
+      } else {
+        if (km) reinterpret_cast<__nv_bfloat16*>(km)[off] = xk;
+        if (kp) reinterpret_cast<__nv_bfloat16*>(kp)[off] = xk;
+        if (vm) reinterpret_cast<__nv_bfloat16*>(vm)[off] = xv;
+        if (vp) reinterpret_cast<__nv_bfloat16*>(vp)[off] = xv;
+      }
+      sum = sum + __bfloat162float(xk);
+    }
+    p.slab_sum[((size_t)layer * p.Lp + pg) * HD + e] = sum;
+  }
+  __syncthreads();
+
+  // phase 3a (fp8, full page): V rows [h][d][0..P) out of shared memory, 16 B at a time
+  if (p.fp8 && full_page) {
+    const int vec_per_row = P / 16;
+    for (int i = tid; i < HD * vec_per_row; i += blockDim.x) {
+      const int e = i / vec_per_row, c = i - e * vec_per_row;
+      const uint4 val = *reinterpret_cast<const uint4*>(vt + (size_t)e * P + c * 16);
+      const size_t off = (size_t)e * P + c * 16;   // e = h*D + d
+      if (vm) *reinterpret_cast<uint4*>(vm + off) = val;
+      if (vp) *reinterpret_cast<uint4*>(vp + off) = val;
+    }
+  }
+
+  // phase 3b: re-quantise the page's slab row
+  const int cnt = p.slab_cnt[(size_t)layer * p.Lp + pg] + R;
+  float amax = 0.0f;
+  for (int e = tid; e < HD; e += blockDim.x) {
+    const float mean = p.slab_sum[((size_t)layer * p.Lp + pg) * HD + e] / (float)cnt;
+    amax = fmaxf(amax, fabsf(mean));
+  }
+  amax = block_max(amax, red);
+  const float s = amax / 127.0f;
+  for (int e = tid; e < HD; e += blockDim.x) {
+    const float mean = p.slab_sum[((size_t)layer * p.Lp + pg) * HD + e] / (float)cnt;
+    int c = 0;
+    if (amax > 0.0f) c = (int)fminf(fmaxf(rintf(mean / s), -127.0f), 127.0f);
+    p.slab[((size_t)layer * p.Lp + pg) * HD + e] = (int8_t)c;
+  }
+  if (tid == 0) {
+    p.slab_cnt[(size_t)layer * p.Lp + pg] = cnt;
+    p.slab_scale[(size_t)layer * p.Lp + pg] = s;
+  }
+}
+
+__global__ void lru_init_kernel(int32_t* slot_of, int32_t* page_of, int32_t* last_use,
+                                int32_t* clock, int Lyr, int Lp, int S, int identity) {
+  const size_t nL = (size_t)Lyr * Lp, nS = (size_t)Lyr * S;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nL; i += stride) {
+    const int pgi = (int)(i % Lp);
+    slot_of[i] = (identity && pgi < S) ? pgi : -1;
+  }
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nS; i += stride) {
+    const int s = (int)(i % S);
+    page_of[i] = (identity && s < Lp) ? s : -1;
+    last_use[i] = -1;
+  }
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)Lyr; i += stride)
+    clock[i] = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_lru_init(const Dims& d, const ssa_cache& c, int identity, cudaStream_t s) {
+  const size_t HD = (size_t)d.Hkv * d.D, n = (size_t)d.Lyr * d.Lp;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(c.slab, 0, n * HD, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(c.slab_sum, 0, n * HD * sizeof(float), s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(c.slab_scale, 0, n * sizeof(float), s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(c.slab_cnt, 0, n * sizeof(int32_t), s)) != cudaSuccess) return e;
+  lru_init_kernel<<<1024, 256, 0, s>>>(c.slot_of, c.page_of, c.last_use, c.clock, d.Lyr, d.Lp,
+                                       d.S, identity);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_store(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                         const void* k, const void* v, const int64_t* pos, int T,
+                         int32_t* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  StoreParams p{};
+  p.k_pool = static_cast<uint8_t*>(c.k_pool);
+  p.v_pool = static_cast<uint8_t*>(c.v_pool);
+  p.k_scale = c.k_scale;
+  p.v_scale = c.v_scale;
+  p.k_mir = static_cast<uint8_t*>(c.k_mirror);
+  p.v_mir = static_cast<uint8_t*>(c.v_mirror);
+  p.k_scale_m = c.k_scale_mirror;
+  p.v_scale_m = c.v_scale_mirror;
+  p.slab = c.slab;
+  p.slab_scale = c.slab_scale;
+  p.slab_sum = c.slab_sum;
+  p.slab_cnt = c.slab_cnt;
+  p.slot_of = c.slot_of;
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.pos = pos;
+  p.T = T;
+  p.status = status;
+  p.layer0 = layer0;
+  p.Lp = d.Lp; p.S = d.S; p.Hkv = d.Hkv; p.D = d.D; p.P = d.P; p.fp8 = d.fp8;
+  const int threads = d.Hkv * d.D > 1024 ? 1024 : d.Hkv * d.D;
+  const size_t smem = d.fp8 ? (size_t)d.Hkv * d.D * d.P : 0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(store_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  store_kernel<<<dim3(T, n_layers), threads, smem, s>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace ssa

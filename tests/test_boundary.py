@@ -1,0 +1,106 @@
+"""The C-ABI boundary, on the CPU: the library builds, loads, exports every
+symbol include/ssa.h declares, and rejects bad arguments on the host with the
+documented codes before anything reaches a GPU (no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ssa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssa_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from sparse_attention_decode_indexer_gb300 import build
+    build.build()
+    import sparse_attention_decode_indexer_gb300 as m
+    return m
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(L.EXPORTS) == set(names)
+
+
+def _layout(L, **kw):
+    base = dict(page_size=64, n_q_heads=16, n_kv_heads=2, head_dim=128, fp8=True, n_layers=2,
+                logical_pages=100, pool_slots=80, batch=1, max_pages=100, block_topk=32)
+    base.update(kw)
+    return L.Layout(**base)
+
+
+def _fake_cache(L, mirror=True):
+    p = ctypes.c_void_p(0x10000)
+    c = L.SsaCache(*([p] * 16))
+    if not mirror:
+        c.k_mirror = c.v_mirror = c.k_scale_mirror = c.v_scale_mirror = None
+    return c
+
+
+def test_workspace_size_and_layout_checks(L):
+    lib = L.lib()
+    good = _layout(L).c()
+    assert lib.ssa_workspace_size(ctypes.byref(good)) > 0
+    for bad in (dict(head_dim=64), dict(page_size=48), dict(n_q_heads=17),
+                dict(n_q_heads=32, n_kv_heads=2), dict(batch=0), dict(block_topk=0)):
+        lay = _layout(L, **bad).c()
+        assert lib.ssa_workspace_size(ctypes.byref(lay)) == 0, bad
+    lay = _layout(L).c()
+    lay.max_sel = 71                          # must be 2k + 8
+    assert lib.ssa_workspace_size(ctypes.byref(lay)) == 0
+    lay = _layout(L).c()
+    lay.kv_dtype = 7
+    assert lib.ssa_workspace_size(ctypes.byref(lay)) == 0
+
+
+def test_host_side_errors_are_returned_before_any_launch(L):
+    lib = L.lib()
+    lay = _layout(L).c()
+    c = _fake_cache(L)
+    p = ctypes.c_void_p(0x10000)
+    # null outputs
+    assert lib.ssa_index_topk(ctypes.byref(lay), ctypes.byref(c), 0, 1, p, p, p, None, p, p, p,
+                              p, None) == -1
+    # layer range past the cache
+    assert lib.ssa_remap_block_table(ctypes.byref(lay), ctypes.byref(c), 1, 2, p, p, p, p,
+                                     None) == -1
+    # pool smaller than one batch selection: 80 < 72 * 2
+    lay2 = _layout(L, batch=2, logical_pages=200, max_pages=100).c()
+    assert lib.ssa_ensure_resident(ctypes.byref(lay2), ctypes.byref(c), 0, 1, p, p, p, p, p, p,
+                                   p, None) == -2
+    # unsupported dtype
+    lay3 = _layout(L).c()
+    lay3.kv_dtype = 9
+    assert lib.ssa_store_kv_mirror(ctypes.byref(lay3), ctypes.byref(c), 0, 1, p, p, p, 4, p,
+                                   None) == -3
+    # a partial mirror
+    c2 = _fake_cache(L)
+    c2.v_scale_mirror = None
+    assert lib.ssa_ensure_resident(ctypes.byref(lay), ctypes.byref(c2), 0, 1, p, p, p, p, p, p,
+                                   p, None) == -4
+
+
+def test_status_strings(L):
+    assert L.status_str(0) == "ok"
+    assert "pool_slots" in L.status_str(-2)
+    assert L.status_str(1 | 8) == "drop|unresolved"
+    assert L.status_str(32) == "timeout"
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path, monkeypatch):
+    import sparse_attention_decode_indexer_gb300 as m
+    monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(m, "_lib", None)
+    with pytest.raises(RuntimeError):
+        m.lib()

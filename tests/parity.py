@@ -56,7 +56,7 @@ def gpu_pool_as_oracle_layout(w: wl.Workload, pool: torch.Tensor, is_v: bool) ->
     if w.fp8 and is_v:
         n = a.shape[0]
         a = a.reshape(n, w.n_kv_heads, w.head_dim, w.page_size).transpose(0, 1, 3, 2)
-        a = np.ascontiguousarray(a).reshape(n, -1)
+        a = np.ascontiguousarray(a).reshape(n, w.n_kv_heads * w.page_size * w.head_dim)
     return a
 
 
@@ -95,7 +95,8 @@ def compare_mirror(w, run, orc, l):
     if w.fp8:
         n = v.shape[0]
         v = np.ascontiguousarray(v.reshape(n, w.n_kv_heads, w.head_dim, w.page_size)
-                                 .transpose(0, 1, 3, 2)).reshape(n, -1)
+                                 .transpose(0, 1, 3, 2)).reshape(n, w.n_kv_heads * w.page_size
+                                                                 * w.head_dim)
     assert np.array_equal(k, orc.k_mirror[l]), "k_mirror"
     assert np.array_equal(v, orc.v_mirror[l]), "v_mirror"
     if w.fp8:

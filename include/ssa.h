@@ -142,7 +142,11 @@ typedef struct ssa_cache {
 
 /* Bytes of scratch (device memory, 256-byte aligned) that ssa_index_topk,
  * ssa_ensure_resident and ssa_sparse_paged_decode need for any layer range
- * of this layout.  The calls use disjoint parts of it.  0 on a bad layout. */
+ * of this layout.  The calls use disjoint parts of it.  Zero the workspace
+ * once before its first use: ssa_sparse_paged_decode keeps per-unit split
+ * counters in it, and every call that completes leaves them zero again (a
+ * call that reported SSA_ST_TIMEOUT may not: zero the workspace again).
+ * 0 on a bad layout. */
 size_t ssa_workspace_size(const ssa_layout *lay);
 
 /*
@@ -247,8 +251,10 @@ int ssa_remap_block_table(const ssa_layout *lay, const ssa_cache *c, int layer0,
  * Entries with sel < 0 are padding; sel >= 0 with phys < 0 are skipped and
  * flagged SSA_ST_UNRESOLVED.  A request with no token gets zeros.
  *   q    [n_layers][B][Hq][D] bf16;  out [n_layers][B][Hq][D] bf16
- * Splits the pages of each (request, KV head) across CTAs and merges the
- * partial softmax states in a second kernel; ws holds the partials.
+ * Splits the pages of each (request, KV head) across CTAs (as many splits as
+ * fill one wave of the GPU); the last CTA of each (layer, request, KV head)
+ * to finish merges the partial softmax states, found by an atomic ticket.
+ * ws holds the partials and the tickets (zeroed before first use).
  */
 int ssa_sparse_paged_decode(const ssa_layout *lay, const ssa_cache *c, int layer0, int n_layers,
                             const void *q, const int32_t *sel, const int32_t *phys,

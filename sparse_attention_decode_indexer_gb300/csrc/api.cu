@@ -86,10 +86,11 @@ int num_sms() {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: [scores | miss_page | miss_slot | n_miss | part_o | part_ml],
-// each sized for the whole layer range of the layout.
+// Workspace: [scores | miss_page | miss_slot | n_miss | part_o | part_ml |
+// tickets], each sized for the whole layer range of the layout.  Only the
+// tickets need a defined start (zero); every call leaves them zero.
 struct WsLayout {
-  size_t scores, miss_page, miss_slot, n_miss, part_o, part_ml, total;
+  size_t scores, miss_page, miss_slot, n_miss, part_o, part_ml, tickets, total;
 };
 
 size_t part_entries(const Dims& d) {
@@ -111,6 +112,7 @@ WsLayout ws_layout(const Dims& d) {
   const size_t pe = part_entries(d);
   w.part_o = off;    off += align256(pe * d.D * 4);
   w.part_ml = off;   off += align256(pe * 2 * 4);
+  w.tickets = off;   off += align256((size_t)d.Lyr * d.B * d.Hkv * 4);
   w.total = off;
   return w;
 }
@@ -250,6 +252,7 @@ int ssa_sparse_paged_decode(const ssa_layout* lay, const ssa_cache* c, int layer
   a.out = out;
   a.part_o = ws ? at<float>(ws, w.part_o) : nullptr;
   a.part_ml = ws ? at<float>(ws, w.part_ml) : nullptr;
+  a.tickets = ws ? at<int32_t>(ws, w.tickets) : nullptr;
   a.status = status;
   cudaError_t e = launch_decode(a, (cudaStream_t)stream);
   return e == cudaSuccess ? SSA_OK : fail_cuda(e);

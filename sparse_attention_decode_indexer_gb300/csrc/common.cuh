@@ -139,12 +139,19 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two e4m3 codes (low 16 bits of v) -> f16x2, exact (e4m3 is a subset of f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
-  uint32_t out;
-  asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\ncvt.rn.f16x2.e4m3x2 %0, lo;\n}"
-      : "=r"(out) : "r"(v16));
-  return out;
+// Four e4m3 codes (one 32-bit word) -> two f16x2: lo = bytes 0,1; hi = bytes
+// 2,3.  Exact: every e4m3 value is an f16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %2;\n"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\ncvt.rn.f16x2.e4m3x2 %1, h;\n}"
+      : "=r"(lo), "=r"(hi) : "r"(w));
+}
+
+// 2^x, hardware approximation (ex2.approx; ~2 ulp, flushes subnormals).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

@@ -69,6 +69,7 @@ struct DecodeParams {
   __nv_bfloat16* out;       // [n_layers][B][Hq][D]
   float* part_o;            // [units][splits][G][D]
   float* part_ml;           // [units][splits][G][2]
+  int32_t* tickets;         // [units] split counters, zero between calls
   int32_t* status;
   int layer0, B, Hq, Hkv, G, W, S, splits;
   float sm_log2;            // sm_scale * log2(e)
@@ -110,6 +111,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   uint64_t* empty = full + NST;
   __shared__ int s_nv;
   __shared__ int s_abort;
+  __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, bh = blockIdx.y, li = blockIdx.z;
@@ -203,9 +205,10 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   }
 
   // ---------------- consumers -------------------------------------------------
+  // QK^T: A = q rows (g = lane/4; rows >= 8 are padding), B = K columns.
+  // PV:   A = V^T rows (d), B = P columns (g), C = O^T[d][g].
   const int g = lane >> 2, c = lane & 3;
 
-  // q fragments (A operand, rows = query heads); fp8 path: scaled to f16 range
   uint32_t qa[8][2];
   float qscale_log2 = p.sm_log2;
   if (FP8) {
@@ -234,12 +237,13 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     }
   }
 
-  float o[16][4];
+  float o[8][4];   // O^T: rows d = 16*mt + g (+8), columns (heads) 2c, 2c+1
 #pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-  // fp8: probabilities carry v_scale / vref, vref a power of two above every
-  // V scale seen so far (0 until the first block sets it)
+  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+  // softmax state of row (head) g; fp8: probabilities carry v_scale / vref,
+  // vref a power of two above every V scale seen so far (0 before the first)
   float m_run = -INFINITY, l_run = 0.0f, vref = FP8 ? 0.0f : 1.0f;
+  const int rot = c >= 2 ? 16 : 0;      // fp8 V: lanes 2, 3 hold the token pairs swapped
 
   for (int st = 0; st < nst; ++st) {
     const int sb = st % NST;
@@ -283,15 +287,22 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
       int tok[4];   // token (within page) of s0[0], s0[1], s1[0], s1[1]
       if (FP8) {
+        // column n of tile t reads token 4*(n/2) + offset: lanes 0,1 of each
+        // quad take token pairs (0,1)/(2,3), lanes 2,3 the reverse, so the
+        // 8 rows a tile reads fall in distinct swizzle chunks (no bank conflict)
         const int nB = lane >> 2, cB = nB >> 1, eB = nB & 1;
         const int t0 = tb + 4 * cB + (cB < 2 ? eB : 2 + eB);
         const int t1 = tb + 4 * cB + (cB < 2 ? 2 + eB : eB);
+        const uint32_t r0 = kb + t0 * 128 + 4 * c, r1 = kb + t1 * 128 + 4 * c;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t w0 = lds32(kb + t0 * 128 + ((ks ^ (t0 & 7)) << 4) + 4 * c);
-          const uint32_t w1 = lds32(kb + t1 * 128 + ((ks ^ (t1 & 7)) << 4) + 4 * c);
-          mma_f16(s0, qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w0 >> 16));
-          mma_f16(s1, qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w1 >> 16));
+          const uint32_t w0 = lds32(r0 + ((ks ^ (t0 & 7)) << 4));
+          const uint32_t w1 = lds32(r1 + ((ks ^ (t1 & 7)) << 4));
+          uint32_t b0, b1, b2, b3;
+          e4m3x4_to_f16x2x2(w0, b0, b1);
+          e4m3x4_to_f16x2x2(w1, b2, b3);
+          mma_f16(s0, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+          mma_f16(s1, qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
         }
         tok[0] = tb + 4 * c + (c < 2 ? 0 : 2);
         tok[1] = tok[0] + 1;
@@ -316,7 +327,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         tok[3] = tok[2] + 1;
       }
 
-      // online softmax (log2 domain), rows g; lanes 4g..4g+3 share a row
+      // online softmax (log2 domain) of row g; lanes 4g..4g+3 share the row
       float x[4] = {s0[0], s0[1], s1[0], s1[1]};
       float vs[4];
       float vmax = 0.0f;
@@ -333,13 +344,13 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_new = fmaxf(m_run, mx);
       const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-      float corr = exp2f(m_run - m_use);
+      const float corr = fast_exp2(m_run - m_use);
       float ocorr = corr;
       if (FP8) {
+        // the 4 lanes of a quad see 4 tokens each, together all 16 of the block
         vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
         vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
         if (vmax >= vref) {
-          // next power of two above vmax; O rescales exactly
           const float nref = __uint_as_float(((__float_as_uint(vmax) >> 23) + 1) << 23);
           ocorr = corr * (vref / nref);
           vref = nref;
@@ -347,12 +358,13 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       }
       float pr[4];
       float lsum = 0.0f;
+      const float vinv = FP8 ? 1.0f / vref : 1.0f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float pi = exp2f(x[i] - m_use);
+        const float pi = fast_exp2(x[i] - m_use);
         if (FP8) {
           lsum += pi;
-          pr[i] = pi * (vs[i] / vref);
+          pr[i] = pi * vs[i] * vinv;
         } else {
           pr[i] = bf16_round(pi);
           lsum += pr[i];
@@ -360,33 +372,43 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       }
       l_run = l_run * corr + lsum;
       m_run = m_new;
+      // O^T columns are heads 2c, 2c+1: their corrections live in quads 2c, 2c+1
+      const float oc0 = __shfl_sync(0xffffffffu, ocorr, (2 * c) * 4);
+      const float oc1 = __shfl_sync(0xffffffffu, ocorr, (2 * c + 1) * 4);
+      if (__any_sync(0xffffffffu, oc0 != 1.0f || oc1 != 1.0f)) {
 #pragma unroll
-      for (int n = 0; n < 16; ++n) { o[n][0] *= ocorr; o[n][1] *= ocorr; }
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= oc0; o[mt][1] *= oc1; o[mt][2] *= oc0; o[mt][3] *= oc1;
+        }
+      }
 
-      // O += P V
+      // O^T += V^T P^T, 16 rows of d per MMA
       if (FP8) {
-        const uint32_t a0 = pack_f16(pr[0], pr[1]), a2 = pack_f16(pr[2], pr[3]);
-        const int dn = lane >> 2;
+        const uint32_t b0 = pack_f16(pr[0], pr[1]), b1 = pack_f16(pr[2], pr[3]);
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          const int d = 8 * n + dn;
-          const uint32_t w = lds32(vb + swz(d * P + tb + 4 * c, C::kVSwz));
-          const uint32_t lo = e4m3x2_to_f16x2(w), hi = e4m3x2_to_f16x2(w >> 16);
-          mma_f16(o[n], a0, 0u, a2, 0u, c < 2 ? lo : hi, c < 2 ? hi : lo);
+        for (int mt = 0; mt < 8; ++mt) {
+          const int d = 16 * mt + g;
+          uint32_t w0 = lds32(vb + swz(d * P + tb + 4 * c, C::kVSwz));
+          uint32_t w1 = lds32(vb + swz((d + 8) * P + tb + 4 * c, C::kVSwz));
+          w0 = __funnelshift_l(w0, w0, rot);
+          w1 = __funnelshift_l(w1, w1, rot);
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(w0, a0, a2);
+          e4m3x4_to_f16x2x2(w1, a1, a3);
+          mma_f16(o[mt], a0, a1, a2, a3, b0, b1);
         }
       } else {
-        const uint32_t a0 = pack_bf16(pr[0], pr[1]), a2 = pack_bf16(pr[2], pr[3]);
+        const uint32_t b0 = pack_bf16(pr[0], pr[1]), b1 = pack_bf16(pr[2], pr[3]);
         const int mi = lane >> 3, r = lane & 7;
-        const int t = tb + (mi & 1) * 8 + r;
+        const int t = tb + (mi >> 1) * 8 + r;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int chunk = 2 * j + (mi >> 1);
+        for (int mt = 0; mt < 8; ++mt) {
+          const int chunk = 2 * mt + (mi & 1);
           const uint32_t addr =
               vb + (chunk >> 3) * (P * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_t(v0, v1, v2, v3, addr);
-          mma_bf16(o[2 * j], a0, 0u, a2, 0u, v0, v1);
-          mma_bf16(o[2 * j + 1], a0, 0u, a2, 0u, v2, v3);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(a0, a1, a2, a3, addr);
+          mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
         }
       }
     }
@@ -402,10 +424,12 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   float* cM = cO + kConsumerWarps * kMaxG * kD;                 // [4][8]
   float* cL = cM + kConsumerWarps * kMaxG;                      // [4][8]
 #pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    const int d = 8 * n + 2 * c;
-    cO[(warp * kMaxG + g) * kD + d] = o[n][0] * vref;
-    cO[(warp * kMaxG + g) * kD + d + 1] = o[n][1] * vref;
+  for (int mt = 0; mt < 8; ++mt) {
+    const int d = 16 * mt + g;
+    cO[(warp * kMaxG + 2 * c) * kD + d] = o[mt][0] * vref;
+    cO[(warp * kMaxG + 2 * c + 1) * kD + d] = o[mt][1] * vref;
+    cO[(warp * kMaxG + 2 * c) * kD + d + 8] = o[mt][2] * vref;
+    cO[(warp * kMaxG + 2 * c + 1) * kD + d + 8] = o[mt][3] * vref;
   }
   if (c == 0) {
     cM[warp * kMaxG + g] = m_run;
@@ -440,30 +464,35 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       }
     }
   }
-}
+  if (p.splits == 1) return;
 
-// a7: combine the splits' (m, l, o) partials of one (layer, request, KV head)
-__global__ void __launch_bounds__(256)
-merge_kernel(const float* part_o, const float* part_ml, __nv_bfloat16* out, int splits,
-             int B, int Hq, int Hkv, int G) {
-  const int unit = blockIdx.x;
-  const int h = unit % Hkv, lb = unit / Hkv;            // lb = li * B + b
-  for (int i = threadIdx.x; i < G * kD; i += blockDim.x) {
-    const int g = i / kD, d = i - g * kD;
+  // ---------------- a7: the last CTA of this unit merges the splits ---------
+  // (an atomic ticket; no CTA ever waits for another)
+  __threadfence();
+  consumer_sync();
+  if (tid == 0) s_last = atomicAdd(&p.tickets[unit], 1) == p.splits - 1;
+  consumer_sync();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = tid; i < p.G * kD; i += kConsumerWarps * 32) {
+    const int gg = i / kD, d = i - gg * kD;
+    const size_t base = (size_t)unit * p.splits * p.G + gg;
     float M = -INFINITY;
-    for (int s = 0; s < splits; ++s)
-      M = fmaxf(M, part_ml[(((size_t)unit * splits + s) * G + g) * 2]);
+    for (int sp = 0; sp < p.splits; ++sp)
+      M = fmaxf(M, __ldcg(&p.part_ml[(base + (size_t)sp * p.G) * 2]));
     float L = 0.0f, O = 0.0f;
     if (M != -INFINITY) {
-      for (int s = 0; s < splits; ++s) {
-        const size_t pi = ((size_t)unit * splits + s) * G + g;
-        const float f = exp2f(part_ml[pi * 2] - M);
-        L += part_ml[pi * 2 + 1] * f;
-        O += part_o[pi * kD + d] * f;
+      for (int sp = 0; sp < p.splits; ++sp) {
+        const size_t pi = base + (size_t)sp * p.G;
+        const float f = exp2f(__ldcg(&p.part_ml[pi * 2]) - M);
+        L += __ldcg(&p.part_ml[pi * 2 + 1]) * f;
+        O += __ldcg(&p.part_o[pi * kD + d]) * f;
       }
     }
-    out[((size_t)lb * Hq + h * G + g) * kD + d] = __float2bfloat16_rn(L > 0.0f ? O / L : 0.0f);
+    p.out[(((size_t)li * p.B + b) * p.Hq + h * p.G + gg) * kD + d] =
+        __float2bfloat16_rn(L > 0.0f ? O / L : 0.0f);
   }
+  if (tid == 0) p.tickets[unit] = 0;     // ready for the next call
 }
 
 // ---------------------------------------------------------------------------
@@ -531,21 +560,37 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeParams& p, cudaStre
   dim3 grid(a.splits, d.B * d.Hkv, a.n_layers);
   decode_kernel<FP8, P><<<grid, kDecodeThreads, smem, s>>>(p, tmK, tmV);
   count_launch();
-  e = cudaGetLastError();
-  if (e != cudaSuccess || a.splits == 1) return e;
-  merge_kernel<<<a.n_layers * d.B * d.Hkv, 256, 0, s>>>(
-      a.part_o, a.part_ml, static_cast<__nv_bfloat16*>(a.out), a.splits, d.B, d.Hq, d.Hkv, d.G);
-  count_launch();
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// Resident CTAs per SM: the register cap of the launch bounds, or the
+// shared-memory footprint, whichever is tighter.
+int decode_ctas_per_sm(const Dims& d) {
+  size_t smem;
+  switch (d.P * 2 + d.fp8) {
+    case 32: smem = decode_smem<false, 16>(d.W); break;
+    case 33: smem = decode_smem<true, 16>(d.W); break;
+    case 64: smem = decode_smem<false, 32>(d.W); break;
+    case 65: smem = decode_smem<true, 32>(d.W); break;
+    case 128: smem = decode_smem<false, 64>(d.W); break;
+    case 129: smem = decode_smem<true, 64>(d.W); break;
+    case 256: smem = decode_smem<false, 128>(d.W); break;
+    default: smem = decode_smem<true, 128>(d.W); break;
+  }
+  const int by_regs = d.fp8 ? 3 : 2;
+  const int by_smem = (int)((228u * 1024u) / (smem + 1024u));
+  return by_smem < 1 ? 1 : (by_smem < by_regs ? by_smem : by_regs);
+}
+
+// Splits of each (layer, request, KV head) unit: as many as fill ONE wave of
+// resident CTAs (a partial second wave would double the tail), at least two
+// pages per split.
 int decode_splits(const Dims& d, int n_layers, int num_sms) {
   const long long units = (long long)n_layers * d.B * d.Hkv;
-  const int ctas_per_sm = d.fp8 ? 3 : 2;
-  const long long target = (long long)num_sms * ctas_per_sm;
-  long long s = (target + units - 1) / units;
+  const long long slots = (long long)num_sms * decode_ctas_per_sm(d);
+  long long s = slots / units;
   const int max_s = d.max_selected() / 2 > 1 ? d.max_selected() / 2 : 1;
   if (s > max_s) s = max_s;
   if (s < 1) s = 1;
@@ -565,6 +610,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.part_o = a.part_o;
   p.part_ml = a.part_ml;
+  p.tickets = a.tickets;
   p.status = a.status;
   p.layer0 = a.layer0;
   p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.G = d.G; p.W = d.W; p.S = d.S;

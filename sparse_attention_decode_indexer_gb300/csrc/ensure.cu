@@ -131,9 +131,14 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
       for (int i = tid; i < 256; i += nt) hist[i] = 0;
       __syncthreads();
       const uint32_t prefix = s_prefix;
-      for (int s = tid; s < p.S; s += nt) {
-        const uint32_t kk = victim_key(page_of, last_use, s, clock);
-        if ((kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255], 1);
+      for (int base = 0; base < p.S; base += nt) {        // uniform trip count
+        const int s = base + tid;
+        const uint32_t kk = s < p.S ? victim_key(page_of, last_use, s, clock) : 0u;
+        const bool use = s < p.S && (kk & mask) == prefix;
+        // one atomic per distinct bin per warp: last_use values cluster
+        const int key = use ? (int)((kk >> shift) & 255) : -1 - (tid & 31);
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (use && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[key], __popc(peers));
       }
       __syncthreads();
       if (tid < 32) {

@@ -42,9 +42,37 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams 
   __shared__ float red[33];
   const int li = blockIdx.z, b = blockIdx.y;
   const int HD = p.Hkv * p.D;
-  const __nv_bfloat16* qb = p.q + ((size_t)li * p.B + b) * p.Hq * p.D;
+  const int L = p.lanes;
+  const int sub = threadIdx.x & (L - 1), grp = threadIdx.x / L;
+  const int groups = blockDim.x / L;
 
-  // q -> int8 with one symmetric scale per request (all heads)
+  // 1. issue this thread's slab loads first: they do not depend on q, so the
+  //    q quantisation below runs while they are in flight
+  const int n_b = min(p.nmax, (p.seq_lens[b] + p.P - 1) / p.P);
+  const int p0 = blockIdx.x * p.pages_per_cta;             // pages_per_cta = groups * iters
+  const int8_t* slab_l = p.slab + (size_t)(p.layer0 + li) * p.Lp * HD;
+  int4 v[kScoreIters][CPL];
+  bool live[kScoreIters];
+#pragma unroll
+  for (int it = 0; it < kScoreIters; ++it) {
+    const int pg = p0 + it * groups + grp;
+    live[it] = false;
+    if (pg < p.nmax && pg < n_b) {
+      const int id = p.bt[(size_t)b * p.nmax + pg];
+      if (id >= 0 && id < p.Lp) {
+        live[it] = true;
+        const int4* row = reinterpret_cast<const int4*>(slab_l + (size_t)id * HD);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) v[it][c] = __ldg(row + sub + c * L);
+      } else if (sub == 0) {
+        set_status(p.status, SSA_ST_BAD_ID);
+      }
+    }
+  }
+
+  // 2. q -> int8 with one symmetric scale per request (all heads), then the
+  //    G query heads of each KV head summed: |sum| <= 127 * G fits int16
+  const __nv_bfloat16* qb = p.q + ((size_t)li * p.B + b) * p.Hq * p.D;
   float amax = 0.0f;
   for (int i = threadIdx.x; i < p.Hq * p.D; i += blockDim.x)
     amax = fmaxf(amax, fabsf(__bfloat162float(qb[i])));
@@ -64,12 +92,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams 
     qg[e] = (int16_t)acc;
   }
   __syncthreads();
-
-  const int L = p.lanes;
-  const int sub = threadIdx.x & (L - 1), grp = threadIdx.x / L;
-  const int groups = blockDim.x / L;
-  // this lane's q pairs, kept in registers for every page
-  int qa[CPL][8];
+  int qa[CPL][8];                  // this lane's q pairs
 #pragma unroll
   for (int c = 0; c < CPL; ++c) {
     const int* q2 = reinterpret_cast<const int*>(qg + (sub + c * L) * 16);
@@ -77,50 +100,36 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams 
     for (int i = 0; i < 8; ++i) qa[c][i] = q2[i];
   }
 
-  const int n_b = min(p.nmax, (p.seq_lens[b] + p.P - 1) / p.P);
-  const int p0 = blockIdx.x * p.pages_per_cta;
-  const int p1 = min(p.nmax, p0 + p.pages_per_cta);
-  const int8_t* slab_l = p.slab + (size_t)(p.layer0 + li) * p.Lp * HD;
+  // 3. exact int32 dot products, reduced over the lanes of each page
   int32_t* out = p.scores + ((size_t)li * p.B + b) * p.nmax;
-
-  for (int base = p0; base < p1; base += groups * kScoreIters) {
-    int4 v[kScoreIters][CPL];
-    bool live[kScoreIters];
 #pragma unroll
-    for (int it = 0; it < kScoreIters; ++it) {
-      const int pg = base + it * groups + grp;
-      live[it] = false;
-      if (pg < p1 && pg < n_b) {
-        const int id = p.bt[(size_t)b * p.nmax + pg];
-        if (id >= 0 && id < p.Lp) {
-          live[it] = true;
-          const int4* row = reinterpret_cast<const int4*>(slab_l + (size_t)id * HD);
+  for (int it = 0; it < kScoreIters; ++it) {
+    const int pg = p0 + it * groups + grp;
+    int acc = 0;
+    if (live[it]) {
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) v[it][c] = __ldg(row + sub + c * L);
-        } else if (sub == 0) {
-          set_status(p.status, SSA_ST_BAD_ID);
+      for (int c = 0; c < CPL; ++c) {
+        const int w[4] = {v[it][c].x, v[it][c].y, v[it][c].z, v[it][c].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc = __dp2a_lo(qa[c][2 * j], w[j], acc);
+          acc = __dp2a_hi(qa[c][2 * j + 1], w[j], acc);
         }
       }
     }
-#pragma unroll
-    for (int it = 0; it < kScoreIters; ++it) {
-      const int pg = base + it * groups + grp;
-      int acc = 0;
-      if (live[it]) {
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          const int w[4] = {v[it][c].x, v[it][c].y, v[it][c].z, v[it][c].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc = __dp2a_lo(qa[c][2 * j], w[j], acc);
-            acc = __dp2a_hi(qa[c][2 * j + 1], w[j], acc);
-          }
-        }
-      }
-      for (int o = L >> 1; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (sub == 0 && pg < p1) out[pg] = live[it] ? acc : INT_MIN;
-    }
+    for (int o = L >> 1; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (sub == 0 && pg < p.nmax) out[pg] = live[it] ? acc : INT_MIN;
   }
+}
+
+// Histogram increment with one atomic per distinct bin per warp (keys often
+// share their top digits, which would serialise plain atomics).  Every lane
+// of the warp must call it; lanes with use == false add nothing.
+__device__ __forceinline__ void hist_add_warp(int* hist, bool use, int bin) {
+  const int lane = threadIdx.x & 31;
+  const int key = use ? bin : -1 - lane;
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  if (use && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
 }
 
 // ---------------------------------------------------------------------------
@@ -161,9 +170,10 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(SelectParams p
       for (int i = tid; i < 256; i += nt) hist[i] = 0;
       __syncthreads();
       const uint32_t prefix = s_prefix;
-      for (int i = tid; i < cand; i += nt) {
-        const uint32_t kk = key[i];
-        if ((kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255], 1);
+      for (int base = 0; base < cand; base += nt) {       // uniform trip count
+        const int i = base + tid;
+        const uint32_t kk = i < cand ? key[i] : 0u;
+        hist_add_warp(hist, i < cand && (kk & mask) == prefix, (int)((kk >> shift) & 255));
       }
       __syncthreads();
       if (tid < 32) {

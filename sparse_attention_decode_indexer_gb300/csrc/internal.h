@@ -63,6 +63,7 @@ struct DecodeArgs {
   void* out;
   float* part_o;   // [units][splits][G][D]
   float* part_ml;  // [units][splits][G][2]
+  int32_t* tickets;  // [units] split counters (zero before the first call; left zero)
   int32_t* status;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);

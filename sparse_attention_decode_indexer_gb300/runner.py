@@ -39,7 +39,8 @@ class DecodeRunner:
         self.out = torch.zeros((L, B, layout.n_q_heads, layout.head_dim), dtype=torch.bfloat16,
                                device=device)
         self.status = torch.zeros((1,), dtype=i32, device=device)
-        self.ws = torch.empty((max(ssa_workspace_size(layout), 256),), dtype=torch.uint8,
+        # zeroed once: the attention keeps split tickets in it and leaves them zero
+        self.ws = torch.zeros((max(ssa_workspace_size(layout), 256),), dtype=torch.uint8,
                               device=device)
         self.sm_scale = 1.0 / math.sqrt(layout.head_dim)
         ssa_lru_init(self.cache, identity)

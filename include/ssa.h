@@ -70,7 +70,9 @@ enum {
   SSA_ERR_POOL_TOO_SMALL = -2,/* pool_slots < min(batch*max_sel, logical)    */
   SSA_ERR_UNSUPPORTED = -3,   /* dtype, page size, head_dim, GQA group       */
   SSA_ERR_NO_MIRROR = -4,     /* a host tier call without mirror pointers    */
-  SSA_ERR_CUDA = -5           /* a CUDA launch or attribute query failed     */
+  SSA_ERR_CUDA = -5,          /* a CUDA launch or attribute query failed     */
+  SSA_ERR_SCRATCH_LIMIT = -6  /* ssa_index_topk_static_scratch: the call needs
+                                 more than SSA_STATIC_SCORE_ENTRIES scores     */
 };
 
 enum {
@@ -260,6 +262,31 @@ int ssa_sparse_paged_decode(const ssa_layout *lay, const ssa_cache *c, int layer
                             const void *q, const int32_t *sel, const int32_t *phys,
                             const int32_t *seq_lens, float sm_scale, void *out,
                             int32_t *status, void *ws, ssa_stream_t stream);
+
+/*
+ * ssa_index_topk without a workspace: the same indexer and top-k selection
+ * (same arguments and results as ssa_index_topk, without scores_opt and ws),
+ * for callers that cannot allocate device memory -- a plugin inside a host
+ * program that owns every device allocation, or a serving loop that must not
+ * allocate after start-up -- and so have no workspace to pass.
+ *
+ * The pages have no counterpart of this call; it only changes where the
+ * score scratch lives.  That scratch is a fixed array of
+ * SSA_STATIC_SCORE_ENTRIES int32 (4 MiB) compiled into the library, held on
+ * every GPU that loads the library until the process exits.  A call needing
+ * more than that (n_layers * batch * max_pages scores) returns
+ * SSA_ERR_SCRATCH_LIMIT before enqueuing anything.  The call allocates and
+ * frees nothing.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it: make that first call before
+ * any stream capture.  Every call uses the same array, which keeps the last
+ * call's scores; nothing in it needs clearing, but calls whose kernels
+ * overlap on the GPU (other streams, other threads) race on it -- order them.
+ */
+#define SSA_STATIC_SCORE_ENTRIES (1u << 20)
+int ssa_index_topk_static_scratch(const ssa_layout *lay, const ssa_cache *c, int layer0,
+                                  int n_layers, const void *q, const int32_t *block_table,
+                                  const int32_t *seq_lens, int32_t *sel, int32_t *n_sel,
+                                  int32_t *status, ssa_stream_t stream);
 
 /* Text for an SSA_ERR_* code or an SSA_ST_* bit set. */
 const char *ssa_status_str(int code);

@@ -31,7 +31,8 @@ ST_DROP, ST_BAD_ID, ST_MISS_NO_MIRROR, ST_UNRESOLVED, ST_BAD_POS, ST_TIMEOUT = 1
 
 EXPORTS = ("ssa_workspace_size", "ssa_lru_init", "ssa_store_kv_mirror", "ssa_index_topk",
            "ssa_ensure_resident", "ssa_remap_block_table", "ssa_sparse_paged_decode",
-           "ssa_status_str", "ssa_last_cuda_error", "ssa_launch_count")
+           "ssa_status_str", "ssa_last_cuda_error", "ssa_launch_count",
+           "ssa_index_topk_static_scratch")
 
 
 class SsaError(RuntimeError):

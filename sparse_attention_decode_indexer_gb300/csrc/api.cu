@@ -126,6 +126,10 @@ T* at(void* ws, size_t off) {
 
 void count_launch(int n) { g_launches += n; }
 
+int validate_layout(const ssa_layout* lay, Dims& d) { return check_layout(lay, d); }
+
+int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
 }  // namespace ssa
 
 using namespace ssa;
@@ -266,6 +270,8 @@ const char* ssa_status_str(int code) {
     case SSA_ERR_UNSUPPORTED: return "unsupported layout (dtype, page size, head_dim, GQA group)";
     case SSA_ERR_NO_MIRROR: return "host mirror pointers incomplete";
     case SSA_ERR_CUDA: return "CUDA launch failed (see ssa_last_cuda_error)";
+    case SSA_ERR_SCRATCH_LIMIT:
+      return "n_layers * batch * max_pages exceeds the static score scratch (SSA_STATIC_SCORE_ENTRIES)";
     default: break;
   }
   if (code > 0) {

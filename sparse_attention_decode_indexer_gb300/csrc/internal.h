@@ -71,4 +71,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 // Counts every kernel launch the library enqueues (per host thread).
 void count_launch(int n = 1);
 
+// Layout validation shared by every entry point (fills the derived view).
+int validate_layout(const ssa_layout* lay, Dims& d);
+
+// Keeps a failed cudaError_t for ssa_last_cuda_error(); returns SSA_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 }  // namespace ssa

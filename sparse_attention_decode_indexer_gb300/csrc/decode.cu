@@ -91,6 +91,19 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// Producer warp -> consumer warps: the page list is written (barrier 2).
+__device__ __forceinline__ void list_publish() {
+  asm volatile("bar.arrive 2, %0;" ::"n"(kDecodeThreads) : "memory");
+}
+__device__ __forceinline__ void list_wait() {
+  asm volatile("bar.sync 2, %0;" ::"n"(kDecodeThreads) : "memory");
+}
+
+// 1/x for x a positive normal power of two, exactly, without a division.
+__device__ __forceinline__ float pow2_rcp(float x) {
+  return __uint_as_float(0x7F000000u - __float_as_uint(x));
+}
+
 __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
@@ -126,8 +139,17 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     s_abort = 0;
     fence_barrier_init();
   }
-  // valid selected pages of this (layer, request), in list order
-  if (warp == 0) {
+  __syncthreads();
+  pdl_wait();                 // sel, phys, q and the pool come from earlier kernels
+  const int seq_len = p.seq_lens[b];
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer warp: the page list, then one elected thread
+    // issues every copy (the consumers meanwhile stage q) ----------------
+    if (lane == 0) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+    }
     const int32_t* selr = p.sel + ((size_t)li * p.B + b) * p.W;
     const int32_t* physr = p.phys + ((size_t)li * p.B + b) * p.W;
     int cnt = 0;
@@ -143,30 +165,10 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       cnt += __popc(m);
     }
     if (lane == 0) s_nv = cnt;
-  }
-  // the G query rows of this KV head (rows >= G are zero)
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.q + (((size_t)li * p.B + b) * p.Hq + (size_t)h * p.G) * kD);
-    uint4* dst = reinterpret_cast<uint4*>(qs);
-    for (int i = tid; i < kMaxG * kD / 8; i += blockDim.x) {
-      const int g = i / (kD / 8);
-      dst[i] = g < p.G ? src[i] : make_uint4(0, 0, 0, 0);
-    }
-  }
-  __syncthreads();
-
-  const int nv = s_nv;
-  const int i0 = (int)((long long)nv * split / p.splits);
-  const int i1 = (int)((long long)nv * (split + 1) / p.splits);
-  const int nst = i1 - i0;
-  const int seq_len = p.seq_lens[b];
-
-  if (warp == kConsumerWarps) {
-    // ---------------- producer: one elected thread issues every copy -------
+    list_publish();           // page list and count visible to the consumers
+    const int i0 = (int)((long long)cnt * split / p.splits);
+    const int nst = (int)((long long)cnt * (split + 1) / p.splits) - i0;
     if (lane != 0 || nst <= 0) return;
-    prefetch_tmap(&tmK);
-    prefetch_tmap(&tmV);
     int issued = 0;
     bool aborted = false;
     for (int st = 0; st < nst; ++st) {
@@ -204,12 +206,27 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     return;
   }
 
-  // ---------------- consumers -------------------------------------------------
-  // QK^T: A = q rows (g = lane/4; rows >= 8 are padding), B = K columns.
-  // PV:   A = V^T rows (d), B = P columns (g), C = O^T[d][g].
-  const int g = lane >> 2, c = lane & 3;
+  // the G query rows of this KV head (rows >= G are zero)
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.q + (((size_t)li * p.B + b) * p.Hq + (size_t)h * p.G) * kD);
+    uint4* dst = reinterpret_cast<uint4*>(qs);
+    for (int i = tid; i < kMaxG * kD / 8; i += kConsumerWarps * 32) {
+      const int g = i / (kD / 8);
+      dst[i] = g < p.G ? src[i] : make_uint4(0, 0, 0, 0);
+    }
+  }
+  consumer_sync();
 
-  uint32_t qa[8][2];
+  // ---------------- consumers -------------------------------------------------
+  // QK^T: A = 16 K rows (tokens), B = q^T (8 heads), C = S^T[token][head].
+  // PV:   A = V^T rows (16 of d), B = P^T (C transposed in registers by
+  //       movmatrix), C = O^T[d][head].  No MMA row is padding.
+  const int r4 = lane >> 2, c = lane & 3;
+
+  // q^T as the B operand: b0 = q[r4][k 2c, 2c+1], b1 = q[r4][k 2c+8, 2c+9];
+  // fp8: logical k pairs map to 4 consecutive bytes of K (d = 16ks+4c..+3)
+  uint32_t qb[8][2];
   float qscale_log2 = p.sm_log2;
   if (FP8) {
     float amax = 0.0f;
@@ -225,25 +242,42 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     qscale_log2 = p.sm_log2 * exp2f((float)-eq);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const __nv_bfloat16* r = qs + g * kD + 16 * ks + 4 * c;
-      qa[ks][0] = pack_f16(__bfloat162float(r[0]) * up, __bfloat162float(r[1]) * up);
-      qa[ks][1] = pack_f16(__bfloat162float(r[2]) * up, __bfloat162float(r[3]) * up);
+      const __nv_bfloat16* r = qs + r4 * kD + 16 * ks + 4 * c;
+      qb[ks][0] = pack_f16(__bfloat162float(r[0]) * up, __bfloat162float(r[1]) * up);
+      qb[ks][1] = pack_f16(__bfloat162float(r[2]) * up, __bfloat162float(r[3]) * up);
     }
   } else {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      qa[ks][0] = *reinterpret_cast<const uint32_t*>(qs + g * kD + 16 * ks + 2 * c);
-      qa[ks][1] = *reinterpret_cast<const uint32_t*>(qs + g * kD + 16 * ks + 2 * c + 8);
+      qb[ks][0] = *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c);
+      qb[ks][1] = *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c + 8);
     }
   }
 
-  float o[8][4];   // O^T: rows d = 16*mt + g (+8), columns (heads) 2c, 2c+1
+  list_wait();              // the producer's page list
+  const int nv = s_nv;
+  const int i0 = (int)((long long)nv * split / p.splits);
+  const int nst = (int)((long long)nv * (split + 1) / p.splits) - i0;
+
+  float o[8][4];   // O^T: rows d = 16*mt + r4 (+8), columns (heads) 2c, 2c+1
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
-  // softmax state of row (head) g; fp8: probabilities carry v_scale / vref,
-  // vref a power of two above every V scale seen so far (0 before the first)
-  float m_run = -INFINITY, l_run = 0.0f, vref = FP8 ? 0.0f : 1.0f;
+  // softmax state of heads 2c, 2c+1 (the lanes that own those O^T columns);
+  // fp8: probabilities carry v_scale / vref, vref a power of two above every
+  // V scale seen so far (0 before the first block)
+  float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.0f, l_run1 = 0.0f;
+  float vref = FP8 ? 0.0f : 1.0f;
   const int rot = c >= 2 ? 16 : 0;      // fp8 V: lanes 2, 3 hold the token pairs swapped
+  // token of MMA row r4 and r4+8 within a 16-token block.  fp8: rows 2j, 2j+1
+  // and 2j+8, 2j+9 cover the 4 consecutive tokens 4j..4j+3 that one 32-bit V
+  // read returns, lanes of j >= 2 taking the pairs swapped so that the 8 rows
+  // one K read touches fall in distinct swizzle chunks (no bank conflicts)
+  int tauA = r4, tauB = r4 + 8;
+  if (FP8) {
+    const int j = r4 >> 1, e = r4 & 1;
+    tauA = 4 * j + (j < 2 ? e : 2 + e);
+    tauB = 4 * j + (j < 2 ? 2 + e : e);
+  }
 
   for (int st = 0; st < nst; ++st) {
     const int sb = st % NST;
@@ -283,113 +317,119 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         __syncwarp();
       }
 
-      // S = Q K^T for 16 tokens: two n8 tiles
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-      int tok[4];   // token (within page) of s0[0], s0[1], s1[0], s1[1]
+      // S^T = K q^T for 16 tokens; even and odd k-steps in two MMA chains
+      float s[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
+      const int tkA = tb + tauA, tkB = tb + tauB;
       if (FP8) {
-        // column n of tile t reads token 4*(n/2) + offset: lanes 0,1 of each
-        // quad take token pairs (0,1)/(2,3), lanes 2,3 the reverse, so the
-        // 8 rows a tile reads fall in distinct swizzle chunks (no bank conflict)
-        const int nB = lane >> 2, cB = nB >> 1, eB = nB & 1;
-        const int t0 = tb + 4 * cB + (cB < 2 ? eB : 2 + eB);
-        const int t1 = tb + 4 * cB + (cB < 2 ? 2 + eB : eB);
-        const uint32_t r0 = kb + t0 * 128 + 4 * c, r1 = kb + t1 * 128 + 4 * c;
+        const uint32_t rA = kb + tkA * 128 + 4 * c, rB = kb + tkB * 128 + 4 * c;
+        const int xA = tkA & 7, xB = tkB & 7;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t w0 = lds32(r0 + ((ks ^ (t0 & 7)) << 4));
-          const uint32_t w1 = lds32(r1 + ((ks ^ (t1 & 7)) << 4));
-          uint32_t b0, b1, b2, b3;
-          e4m3x4_to_f16x2x2(w0, b0, b1);
-          e4m3x4_to_f16x2x2(w1, b2, b3);
-          mma_f16(s0, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-          mma_f16(s1, qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+        for (int ks = 0; ks < 8; ks += 2) {
+          const uint32_t wA0 = lds32(rA + ((ks ^ xA) << 4));
+          const uint32_t wB0 = lds32(rB + ((ks ^ xB) << 4));
+          const uint32_t wA1 = lds32(rA + (((ks + 1) ^ xA) << 4));
+          const uint32_t wB1 = lds32(rB + (((ks + 1) ^ xB) << 4));
+          uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+          e4m3x4_to_f16x2x2(wA0, a0, a2);
+          e4m3x4_to_f16x2x2(wB0, a1, a3);
+          e4m3x4_to_f16x2x2(wA1, a4, a6);
+          e4m3x4_to_f16x2x2(wB1, a5, a7);
+          mma_f16(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          mma_f16(sx, a4, a5, a6, a7, qb[ks + 1][0], qb[ks + 1][1]);
         }
-        tok[0] = tb + 4 * c + (c < 2 ? 0 : 2);
-        tok[1] = tok[0] + 1;
-        tok[2] = tb + 4 * c + (c < 2 ? 2 : 0);
-        tok[3] = tok[2] + 1;
       } else {
-        const int mi = lane >> 3, r = lane & 7;
-        const int t = tb + (mi >> 1) * 8 + r;
+        const int mi = lane >> 3, rr = lane & 7;
+        const int t = tb + (mi & 1) * 8 + rr;
+        const uint32_t rowk = kb + t * 128;
+        const int xt = t & 7;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const int chunk = 2 * ks + (mi & 1);
-          const uint32_t addr =
-              kb + (chunk >> 3) * (P * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(b0, b1, b2, b3, addr);
-          mma_bf16(s0, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-          mma_bf16(s1, qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+        for (int ks = 0; ks < 8; ks += 2) {
+          uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+          const int c0 = 2 * ks + (mi >> 1), c1 = c0 + 2;     // 16-byte chunks over d
+          ldsm_x4(a0, a1, a2, a3, rowk + (c0 >> 3) * (P * 128) + (((c0 & 7) ^ xt) << 4));
+          ldsm_x4(a4, a5, a6, a7, rowk + (c1 >> 3) * (P * 128) + (((c1 & 7) ^ xt) << 4));
+          mma_bf16(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+          mma_bf16(sx, a4, a5, a6, a7, qb[ks + 1][0], qb[ks + 1][1]);
         }
-        tok[0] = tb + 2 * c;
-        tok[1] = tok[0] + 1;
-        tok[2] = tb + 8 + 2 * c;
-        tok[3] = tok[2] + 1;
       }
-
-      // online softmax (log2 domain) of row g; lanes 4g..4g+3 share the row
-      float x[4] = {s0[0], s0[1], s1[0], s1[1]};
-      float vs[4];
-      float vmax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const bool valid = tok[i] < nvalid;
-        const float ksc_i = FP8 ? ksc[tok[i]] : 1.0f;
-        x[i] = valid ? x[i] * ksc_i * qscale_log2 : -INFINITY;
-        vs[i] = (FP8 && valid) ? vsc[tok[i]] : 0.0f;
-        vmax = fmaxf(vmax, vs[i]);
-      }
-      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-      const float corr = fast_exp2(m_run - m_use);
-      float ocorr = corr;
+      // rows: s[0], s[1] = token tkA, heads 2c, 2c+1; s[2], s[3] = token tkB
+      float x0 = (s[0] + sx[0]) * qscale_log2, x1 = (s[1] + sx[1]) * qscale_log2;
+      float x2 = (s[2] + sx[2]) * qscale_log2, x3 = (s[3] + sx[3]) * qscale_log2;
+      float vsA = 0.0f, vsB = 0.0f;
       if (FP8) {
-        // the 4 lanes of a quad see 4 tokens each, together all 16 of the block
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+        const float kA = ksc[tkA], kB = ksc[tkB];
+        x0 *= kA; x1 *= kA; x2 *= kB; x3 *= kB;
+        vsA = vsc[tkA];
+        vsB = vsc[tkB];
+      }
+      if (nvalid < tb + 16) {          // the tail of a request's last page
+        if (tkA >= nvalid) { x0 = x1 = -INFINITY; vsA = 0.0f; }
+        if (tkB >= nvalid) { x2 = x3 = -INFINITY; vsB = 0.0f; }
+      }
+      // per-head maxima over the 16 tokens: the 8 lanes r4 = 0..7 of this c
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
+      const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
+      const float corr0 = fast_exp2(m_run0 - mu0), corr1 = fast_exp2(m_run1 - mu1);
+      float oc0 = corr0, oc1 = corr1;
+      float vinv = 1.0f;
+      if (FP8) {
+        float vmax = fmaxf(vsA, vsB);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1)
+          vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
         if (vmax >= vref) {
           const float nref = __uint_as_float(((__float_as_uint(vmax) >> 23) + 1) << 23);
-          ocorr = corr * (vref / nref);
+          const float ratio = vref * pow2_rcp(nref);
+          oc0 *= ratio;
+          oc1 *= ratio;
           vref = nref;
         }
+        vinv = pow2_rcp(vref);
       }
-      float pr[4];
-      float lsum = 0.0f;
-      const float vinv = FP8 ? 1.0f / vref : 1.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float pi = fast_exp2(x[i] - m_use);
-        if (FP8) {
-          lsum += pi;
-          pr[i] = pi * vs[i] * vinv;
-        } else {
-          pr[i] = bf16_round(pi);
-          lsum += pr[i];
-        }
+      const float p0 = fast_exp2(x0 - mu0), p1 = fast_exp2(x1 - mu1);
+      const float p2 = fast_exp2(x2 - mu0), p3 = fast_exp2(x3 - mu1);
+      uint32_t P0, P1;
+      if (FP8) {
+        l_run0 = l_run0 * corr0 + (p0 + p2);
+        l_run1 = l_run1 * corr1 + (p1 + p3);
+        const float wA = vsA * vinv, wB = vsB * vinv;
+        P0 = pack_f16(p0 * wA, p1 * wA);
+        P1 = pack_f16(p2 * wB, p3 * wB);
+      } else {
+        const float q0 = bf16_round(p0), q1 = bf16_round(p1);
+        const float q2 = bf16_round(p2), q3 = bf16_round(p3);
+        l_run0 = l_run0 * corr0 + (q0 + q2);
+        l_run1 = l_run1 * corr1 + (q1 + q3);
+        P0 = pack_bf16(q0, q1);
+        P1 = pack_bf16(q2, q3);
       }
-      l_run = l_run * corr + lsum;
-      m_run = m_new;
-      // O^T columns are heads 2c, 2c+1: their corrections live in quads 2c, 2c+1
-      const float oc0 = __shfl_sync(0xffffffffu, ocorr, (2 * c) * 4);
-      const float oc1 = __shfl_sync(0xffffffffu, ocorr, (2 * c + 1) * 4);
+      m_run0 = mn0;
+      m_run1 = mn1;
       if (__any_sync(0xffffffffu, oc0 != 1.0f || oc1 != 1.0f)) {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           o[mt][0] *= oc0; o[mt][1] *= oc1; o[mt][2] *= oc0; o[mt][3] *= oc1;
         }
       }
+      // P^T as the B operand: each 8x8 half transposed across the warp
+      const uint32_t b0 = movmatrix_trans(P0), b1 = movmatrix_trans(P1);
 
       // O^T += V^T P^T, 16 rows of d per MMA
       if (FP8) {
-        const uint32_t b0 = pack_f16(pr[0], pr[1]), b1 = pack_f16(pr[2], pr[3]);
+        // rows d = 16*mt + r4 and +8: the swizzle bits do not depend on mt
+        // (16*P*mt is a multiple of the swizzle period), so hoist them
+        const uint32_t va0 = vb + swz(r4 * P + tb + 4 * c, C::kVSwz);
+        const uint32_t va1 = vb + swz((r4 + 8) * P + tb + 4 * c, C::kVSwz);
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          const int d = 16 * mt + g;
-          uint32_t w0 = lds32(vb + swz(d * P + tb + 4 * c, C::kVSwz));
-          uint32_t w1 = lds32(vb + swz((d + 8) * P + tb + 4 * c, C::kVSwz));
+          uint32_t w0 = lds32(va0 + mt * 16 * P);
+          uint32_t w1 = lds32(va1 + mt * 16 * P);
           w0 = __funnelshift_l(w0, w0, rot);
           w1 = __funnelshift_l(w1, w1, rot);
           uint32_t a0, a1, a2, a3;
@@ -398,9 +438,8 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           mma_f16(o[mt], a0, a1, a2, a3, b0, b1);
         }
       } else {
-        const uint32_t b0 = pack_bf16(pr[0], pr[1]), b1 = pack_bf16(pr[2], pr[3]);
-        const int mi = lane >> 3, r = lane & 7;
-        const int t = tb + (mi >> 1) * 8 + r;
+        const int mi = lane >> 3, rr = lane & 7;
+        const int t = tb + (mi >> 1) * 8 + rr;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           const int chunk = 2 * mt + (mi & 1);
@@ -417,23 +456,29 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   }
 
   // ---------------- merge the 4 warps' states (stage ring is idle now) ------
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  // l: sum over the 8 lanes (r4) that share heads 2c, 2c+1
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
+    l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
+  }
   consumer_sync();
   float* cO = reinterpret_cast<float*>(ring);                  // [4][8][D]
   float* cM = cO + kConsumerWarps * kMaxG * kD;                 // [4][8]
   float* cL = cM + kConsumerWarps * kMaxG;                      // [4][8]
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    const int d = 16 * mt + g;
+    const int d = 16 * mt + r4;
     cO[(warp * kMaxG + 2 * c) * kD + d] = o[mt][0] * vref;
     cO[(warp * kMaxG + 2 * c + 1) * kD + d] = o[mt][1] * vref;
     cO[(warp * kMaxG + 2 * c) * kD + d + 8] = o[mt][2] * vref;
     cO[(warp * kMaxG + 2 * c + 1) * kD + d + 8] = o[mt][3] * vref;
   }
-  if (c == 0) {
-    cM[warp * kMaxG + g] = m_run;
-    cL[warp * kMaxG + g] = l_run;
+  if (r4 == 0) {
+    cM[warp * kMaxG + 2 * c] = m_run0;
+    cM[warp * kMaxG + 2 * c + 1] = m_run1;
+    cL[warp * kMaxG + 2 * c] = l_run0;
+    cL[warp * kMaxG + 2 * c + 1] = l_run1;
   }
   consumer_sync();
   const int unit = (li * p.B + b) * p.Hkv + h;
@@ -447,7 +492,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float f = exp2f(cM[w * kMaxG + gg] - M);
+        const float f = fast_exp2(cM[w * kMaxG + gg] - M);
         L += cL[w * kMaxG + gg] * f;
         O += cO[(w * kMaxG + gg) * kD + d] * f;
       }
@@ -474,23 +519,33 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   consumer_sync();
   if (!s_last) return;
   __threadfence();
-  for (int i = tid; i < p.G * kD; i += kConsumerWarps * 32) {
-    const int gg = i / kD, d = i - gg * kD;
-    const size_t base = (size_t)unit * p.splits * p.G + gg;
+  // one pass: per head, the splits' weights exp2(m_s - M) and 1/L in shared
+  // memory (the ring is idle), then every output sums its splits' partials
+  float* sF = reinterpret_cast<float*>(ring);              // [splits][8]
+  float* sInvL = sF + p.splits * kMaxG;                     // [8]
+  const size_t ub = (size_t)unit * p.splits * p.G;
+  if (tid < p.G) {
     float M = -INFINITY;
     for (int sp = 0; sp < p.splits; ++sp)
-      M = fmaxf(M, __ldcg(&p.part_ml[(base + (size_t)sp * p.G) * 2]));
-    float L = 0.0f, O = 0.0f;
-    if (M != -INFINITY) {
-      for (int sp = 0; sp < p.splits; ++sp) {
-        const size_t pi = base + (size_t)sp * p.G;
-        const float f = exp2f(__ldcg(&p.part_ml[pi * 2]) - M);
-        L += __ldcg(&p.part_ml[pi * 2 + 1]) * f;
-        O += __ldcg(&p.part_o[pi * kD + d]) * f;
-      }
+      M = fmaxf(M, __ldcg(&p.part_ml[(ub + (size_t)sp * p.G + tid) * 2]));
+    float L = 0.0f;
+    for (int sp = 0; sp < p.splits; ++sp) {
+      const size_t pi = ub + (size_t)sp * p.G + tid;
+      const float f = M == -INFINITY ? 0.0f : fast_exp2(__ldcg(&p.part_ml[pi * 2]) - M);
+      sF[sp * kMaxG + tid] = f;
+      L += __ldcg(&p.part_ml[pi * 2 + 1]) * f;
     }
+    sInvL[tid] = L > 0.0f ? 1.0f / L : 0.0f;
+  }
+  consumer_sync();
+  for (int i = tid; i < p.G * kD; i += kConsumerWarps * 32) {
+    const int gg = i / kD, d = i - gg * kD;
+    float O = 0.0f;
+#pragma unroll 4
+    for (int sp = 0; sp < p.splits; ++sp)
+      O += sF[sp * kMaxG + gg] * __ldcg(&p.part_o[(ub + (size_t)sp * p.G + gg) * kD + d]);
     p.out[(((size_t)li * p.B + b) * p.Hq + h * p.G + gg) * kD + d] =
-        __float2bfloat16_rn(L > 0.0f ? O / L : 0.0f);
+        __float2bfloat16_rn(O * sInvL[gg]);
   }
   if (tid == 0) p.tickets[unit] = 0;     // ready for the next call
 }
@@ -558,9 +613,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeParams& p, cudaStre
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.splits, d.B * d.Hkv, a.n_layers);
-  decode_kernel<FP8, P><<<grid, kDecodeThreads, smem, s>>>(p, tmK, tmV);
+  e = launch_pdl(decode_kernel<FP8, P>, grid, dim3(kDecodeThreads), smem, s, p, tmK, tmV);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
   __shared__ int tmp[33];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining, s_nv;
+  pdl_wait();
 
   const int li = blockIdx.x, layer = p.layer0 + li;
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -238,6 +239,7 @@ struct CopyParams {
 };
 
 __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(CopyParams p) {
+  pdl_wait();
   const int entry = blockIdx.y, li = blockIdx.z, layer = p.layer0 + li;
   if (entry >= p.n_miss[li] || p.k_mir == nullptr) return;
   const int pg = p.miss_page[(size_t)li * p.BW + entry];
@@ -289,6 +291,7 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(CopyParams p) {
 __global__ void remap_kernel(const int32_t* slot_of, const int32_t* sel, const int32_t* bt,
                              int32_t* phys, int32_t* status, int layer0, int n_layers, int Lp,
                              int B, int W, int nmax) {
+  pdl_wait();
   const long long n = (long long)n_layers * B * W;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -331,9 +334,9 @@ cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, i
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  ensure_state_kernel<<<n_layers, kEnsureThreads, smem, s>>>(p);
+  cudaError_t e = launch_pdl(ensure_state_kernel, dim3(n_layers), dim3(kEnsureThreads), smem, s, p);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
@@ -352,9 +355,9 @@ cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int 
   p.page_bytes = (long long)d.page_bytes();
   const long long total16 = 2 * p.page_bytes / 16 + (d.fp8 ? 2LL * d.P * 4 / 16 : 0);
   dim3 grid((unsigned)((total16 + kCopyChunk - 1) / kCopyChunk), p.BW, n_layers);
-  miss_copy_kernel<<<grid, kCopyThreads, 0, s>>>(p);
+  cudaError_t e = launch_pdl(miss_copy_kernel, grid, dim3(kCopyThreads), 0, s, p);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_remap(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
@@ -363,10 +366,11 @@ cudaError_t launch_remap(const Dims& d, const ssa_cache& c, int layer0, int n_la
   const long long n = (long long)n_layers * d.B * d.W;
   const int threads = 256;
   const int blocks = (int)((n + threads - 1) / threads);
-  remap_kernel<<<blocks, threads, 0, s>>>(c.slot_of, sel, bt, phys, status, layer0, n_layers,
-                                          d.Lp, d.B, d.W, d.nmax);
+  cudaError_t e = launch_pdl(remap_kernel, dim3(blocks), dim3(threads), 0, s,
+                             (const int32_t*)c.slot_of, sel, bt, phys, status, layer0, n_layers,
+                             d.Lp, d.B, d.W, d.nmax);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace ssa

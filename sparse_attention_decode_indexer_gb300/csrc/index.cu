@@ -40,6 +40,7 @@ template <int CPL>
 __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams p) {
   extern __shared__ int16_t qg[];  // [Hkv][D] group sums of q8
   __shared__ float red[33];
+  pdl_wait();
   const int li = blockIdx.z, b = blockIdx.y;
   const int HD = p.Hkv * p.D;
   const int L = p.lanes;
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(SelectParams p
   __shared__ int tmp[33];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
+  pdl_wait();
   const int b = blockIdx.x, li = blockIdx.y;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int n = min(p.nmax, (p.seq_lens[b] + p.P - 1) / p.P);
@@ -276,12 +278,10 @@ cudaError_t launch_index_scores(const Dims& d, const ssa_cache& c, int layer0, i
   p.pages_per_cta = kScoreIters * (kScoreThreads / p.lanes);
   dim3 grid((d.nmax + p.pages_per_cta - 1) / p.pages_per_cta, d.B, n_layers);
   const size_t smem = (size_t)d.Hkv * d.D * sizeof(int16_t);
-  if (cpl == 1)
-    index_score_kernel<1><<<grid, kScoreThreads, smem, s>>>(p);
-  else
-    index_score_kernel<2><<<grid, kScoreThreads, smem, s>>>(p);
+  cudaError_t e = cpl == 1 ? launch_pdl(index_score_kernel<1>, grid, dim3(kScoreThreads), smem, s, p)
+                           : launch_pdl(index_score_kernel<2>, grid, dim3(kScoreThreads), smem, s, p);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_topk_select(const Dims& d, int n_layers, const int32_t* scores,
@@ -294,9 +294,9 @@ cudaError_t launch_topk_select(const Dims& d, int n_layers, const int32_t* score
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  topk_select_kernel<<<dim3(d.B, n_layers), kSelThreads, smem, s>>>(p);
+  cudaError_t e = launch_pdl(topk_select_kernel, dim3(d.B, n_layers), dim3(kSelThreads), smem, s, p);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace ssa

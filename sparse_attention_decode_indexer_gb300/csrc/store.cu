@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
   __shared__ int s_j[kMaxPage];
   __shared__ int s_run;
   __shared__ float red[33];
+  pdl_wait();
   const int t0 = blockIdx.x, li = blockIdx.y, layer = p.layer0 + li;
   const int tid = threadIdx.x, P = p.P, HD = p.Hkv * p.D;
 
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
 
 __global__ void lru_init_kernel(int32_t* slot_of, int32_t* page_of, int32_t* last_use,
                                 int32_t* clock, int Lyr, int Lp, int S, int identity) {
+  pdl_wait();
   const size_t nL = (size_t)Lyr * Lp, nS = (size_t)Lyr * S;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nL; i += stride) {
@@ -217,10 +219,10 @@ cudaError_t launch_lru_init(const Dims& d, const ssa_cache& c, int identity, cud
   if ((e = cudaMemsetAsync(c.slab_sum, 0, n * HD * sizeof(float), s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(c.slab_scale, 0, n * sizeof(float), s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(c.slab_cnt, 0, n * sizeof(int32_t), s)) != cudaSuccess) return e;
-  lru_init_kernel<<<1024, 256, 0, s>>>(c.slot_of, c.page_of, c.last_use, c.clock, d.Lyr, d.Lp,
-                                       d.S, identity);
+  e = launch_pdl(lru_init_kernel, dim3(1024), dim3(256), 0, s, c.slot_of, c.page_of, c.last_use,
+                 c.clock, d.Lyr, d.Lp, d.S, identity);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_store(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
@@ -255,9 +257,9 @@ cudaError_t launch_store(const Dims& d, const ssa_cache& c, int layer0, int n_la
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  store_kernel<<<dim3(T, n_layers), threads, smem, s>>>(p);
+  cudaError_t e = launch_pdl(store_kernel, dim3(T, n_layers), dim3(threads), smem, s, p);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace ssa

@@ -201,7 +201,9 @@ int ssa_store_kv_mirror(const ssa_layout *lay, const ssa_cache *c, int layer0, i
  * Selection: the k best of pages [0, n_b - 1) by (score desc, page asc),
  * plus page n_b - 1 always; all pages when n_b - 1 <= k.  Selections that
  * would not fit W are dropped and flagged SSA_ST_DROP (cannot happen when
- * W = 2k + 8).  ws: ssa_workspace_size bytes.
+ * W = 2k + 8).  One launch: the last CTA to finish scoring a (layer,
+ * request) row selects over it.  ws: ssa_workspace_size bytes, zeroed once
+ * (required; it holds the per-row tickets).
  */
 int ssa_index_topk(const ssa_layout *lay, const ssa_cache *c, int layer0, int n_layers,
                    const void *q, const int32_t *block_table, const int32_t *seq_lens,
@@ -287,6 +289,15 @@ int ssa_index_topk_static_scratch(const ssa_layout *lay, const ssa_cache *c, int
                                   int n_layers, const void *q, const int32_t *block_table,
                                   const int32_t *seq_lens, int32_t *sel, int32_t *n_sel,
                                   int32_t *status, ssa_stream_t stream);
+
+/*
+ * Failure-detection self-test (no counterpart in the pages): one CTA waits on
+ * an mbarrier that nothing ever arrives on, using the bounded wait of every
+ * kernel in this library (1 s of wall clock).  The wait gives up, the kernel
+ * ORs SSA_ST_TIMEOUT into *status (device memory) and returns; the context
+ * stays usable.  Takes about one second of GPU time.
+ */
+int ssa_selftest_bounded_wait(int32_t *status, ssa_stream_t stream);
 
 /* Text for an SSA_ERR_* code or an SSA_ST_* bit set. */
 const char *ssa_status_str(int code);

@@ -32,7 +32,7 @@ ST_DROP, ST_BAD_ID, ST_MISS_NO_MIRROR, ST_UNRESOLVED, ST_BAD_POS, ST_TIMEOUT = 1
 EXPORTS = ("ssa_workspace_size", "ssa_lru_init", "ssa_store_kv_mirror", "ssa_index_topk",
            "ssa_ensure_resident", "ssa_remap_block_table", "ssa_sparse_paged_decode",
            "ssa_status_str", "ssa_last_cuda_error", "ssa_launch_count",
-           "ssa_index_topk_static_scratch")
+           "ssa_index_topk_static_scratch", "ssa_selftest_bounded_wait")
 
 
 class SsaError(RuntimeError):
@@ -87,6 +87,8 @@ def lib():
         L.ssa_last_cuda_error.argtypes = []
         L.ssa_launch_count.restype = ctypes.c_longlong
         L.ssa_launch_count.argtypes = []
+        L.ssa_selftest_bounded_wait.restype = i32
+        L.ssa_selftest_bounded_wait.argtypes = [vp, vp]
         _lib = L
     return _lib
 
@@ -247,6 +249,12 @@ def ssa_sparse_paged_decode(cache: KVCache, layer0: int, n_layers: int, q, sel, 
                                          n_layers, _ptr(q), _ptr(sel), _ptr(phys),
                                          _ptr(seq_lens), float(sm_scale), _ptr(out),
                                          _ptr(status), _ptr(ws), _stream(stream)))
+
+
+def ssa_selftest_bounded_wait(status, stream=None):
+    """One CTA waits on an mbarrier nothing arrives on; the bounded wait gives
+    up after about a second and sets ST_TIMEOUT in ``status``."""
+    _check(lib().ssa_selftest_bounded_wait(_ptr(status), _stream(stream)))
 
 
 def launch_count() -> int:

@@ -87,10 +87,11 @@ int num_sms() {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace: [scores | miss_page | miss_slot | n_miss | part_o | part_ml |
-// tickets], each sized for the whole layer range of the layout.  Only the
-// tickets need a defined start (zero); every call leaves them zero.
+// tickets | idx_tickets], each sized for the whole layer range of the
+// layout.  Only the tickets need a defined start (zero); every call leaves
+// them zero.
 struct WsLayout {
-  size_t scores, miss_page, miss_slot, n_miss, part_o, part_ml, tickets, total;
+  size_t scores, miss_page, miss_slot, n_miss, part_o, part_ml, tickets, idx_tickets, total;
 };
 
 size_t part_entries(const Dims& d) {
@@ -113,6 +114,7 @@ WsLayout ws_layout(const Dims& d) {
   w.part_o = off;    off += align256(pe * d.D * 4);
   w.part_ml = off;   off += align256(pe * 2 * 4);
   w.tickets = off;   off += align256((size_t)d.Lyr * d.B * d.Hkv * 4);
+  w.idx_tickets = off; off += align256((size_t)d.Lyr * d.B * 4);
   w.total = off;
   return w;
 }
@@ -178,14 +180,12 @@ int ssa_index_topk(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_
   if (!c || !c->slab) return SSA_ERR_INVALID_ARG;
   if ((r = check_range(d, layer0, n_layers))) return r;
   if (!q || !block_table || !seq_lens || !sel || !n_sel) return SSA_ERR_INVALID_ARG;
-  if (!scores_opt && !ws) return SSA_ERR_INVALID_ARG;
+  if (!ws) return SSA_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(d);
   int32_t* scores = scores_opt ? scores_opt : at<int32_t>(ws, w.scores);
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_index_scores(d, *c, layer0, n_layers, q, block_table, seq_lens, scores,
-                                      status, s);
-  if (e != cudaSuccess) return fail_cuda(e);
-  e = launch_topk_select(d, n_layers, scores, seq_lens, sel, n_sel, status, s);
+  cudaError_t e = launch_index_topk(d, *c, layer0, n_layers, q, block_table, seq_lens, scores,
+                                    sel, n_sel, at<int32_t>(ws, w.idx_tickets), status,
+                                    (cudaStream_t)stream);
   return e == cudaSuccess ? SSA_OK : fail_cuda(e);
 }
 

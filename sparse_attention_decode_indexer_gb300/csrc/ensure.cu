@@ -65,11 +65,20 @@ __device__ __forceinline__ uint32_t victim_key(const int32_t* page_of, const int
   return (uint32_t)k ^ 0x80000000u;
 }
 
+// Up to this many slots, the victim keys are read from global memory once and
+// kept in shared memory; beyond it every radix pass reads them again.
+constexpr int kSmemKeys = 16384;
+// Up to this many misses, the victim order is found by all-pairs ranking
+// (one pass, one barrier); beyond it by a bitonic sort.
+constexpr int kRankMax = 1024;
+
+template <bool KEYS_IN_SMEM>
 __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsureParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const int N2 = p.N2;
-  uint64_t* vic = reinterpret_cast<uint64_t*>(smem_raw);            // [N2]
-  uint32_t* ids = reinterpret_cast<uint32_t*>(smem_raw + (size_t)N2 * 8);  // [N2]
+  uint64_t* vic = reinterpret_cast<uint64_t*>(smem_raw);                   // [N2]
+  uint32_t* ids = reinterpret_cast<uint32_t*>(smem_raw + (size_t)N2 * 8);   // [N2]
+  uint32_t* keys = ids + N2;                                                 // [S] (KEYS_IN_SMEM)
   __shared__ int hist[256];
   __shared__ int tmp[33];
   __shared__ uint32_t s_prefix;
@@ -126,7 +135,13 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
 
   if (m > 0) {
     // 3. the m smallest victim keys: MSB-first radix select on 32-bit keys
+    if (KEYS_IN_SMEM) {
+      for (int s = tid; s < p.S; s += nt) keys[s] = victim_key(page_of, last_use, s, clock);
+    }
     if (tid == 0) { s_prefix = 0; s_remaining = m; s_nv = 0; }
+    auto key_of = [&](int s) -> uint32_t {
+      return KEYS_IN_SMEM ? keys[s] : victim_key(page_of, last_use, s, clock);
+    };
     uint32_t mask = 0;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += nt) hist[i] = 0;
@@ -134,7 +149,7 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
       const uint32_t prefix = s_prefix;
       for (int base = 0; base < p.S; base += nt) {        // uniform trip count
         const int s = base + tid;
-        const uint32_t kk = s < p.S ? victim_key(page_of, last_use, s, clock) : 0u;
+        const uint32_t kk = s < p.S ? key_of(s) : 0u;
         const bool use = s < p.S && (kk & mask) == prefix;
         // one atomic per distinct bin per warp: last_use values cluster
         const int key = use ? (int)((kk >> shift) & 255) : -1 - (tid & 31);
@@ -177,7 +192,7 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
     const int s0 = min(p.S, tid * sper), s1 = min(p.S, s0 + sper);
     int eq = 0;
     for (int s = s0; s < s1; ++s) {
-      const uint32_t kk = victim_key(page_of, last_use, s, clock);
+      const uint32_t kk = key_of(s);
       if (kk < T) vic[atomicAdd(&s_nv, 1)] = ((uint64_t)kk << 32) | (uint32_t)s;
       else if (kk == T) ++eq;
     }
@@ -185,22 +200,36 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
     int er = block_exclusive_scan(eq, tmp, eqtot);
     const int n_lt = m - need_eq;
     for (int s = s0; s < s1 && er < need_eq; ++s) {
-      const uint32_t kk = victim_key(page_of, last_use, s, clock);
+      const uint32_t kk = key_of(s);
       if (kk == T) {
         if (er < need_eq) vic[n_lt + er] = ((uint64_t)kk << 32) | (uint32_t)s;
         ++er;
       }
     }
-    int M2 = 1;
-    while (M2 < m) M2 <<= 1;
-    for (int i = m + tid; i < M2; i += nt) vic[i] = ~0ull;
     __syncthreads();
-    bitonic_sort_smem(vic, M2);
+    // 4. victim order: (key, slot) ascending.  The keys are distinct (slots
+    //    are), so each victim's rank is the count of smaller keys.
+    if (m <= kRankMax) {
+      for (int i = tid; i < m; i += nt) {
+        const uint64_t x = vic[i];
+        int r = 0;
+        for (int j = 0; j < m; ++j) r += vic[j] < x;
+        ids[r] = (uint32_t)(x & 0xFFFFFFFFu);      // ids are no longer needed
+      }
+    } else {
+      int M2 = 1;
+      while (M2 < m) M2 <<= 1;
+      for (int i = m + tid; i < M2; i += nt) vic[i] = ~0ull;
+      __syncthreads();
+      bitonic_sort_smem(vic, M2);
+      for (int i = tid; i < m; i += nt) ids[i] = (uint32_t)(vic[i] & 0xFFFFFFFFu);
+    }
+    __syncthreads();
 
-    // 4. rebind: i-th miss takes the i-th victim
+    // 5. rebind: i-th miss takes the i-th victim
     for (int i = tid; i < m; i += nt) {
       const int pg = mpage[i];
-      const int v = (int)(uint32_t)(vic[i] & 0xFFFFFFFFu);
+      const int v = (int)ids[i];
       const int old = page_of[v];
       if (old >= 0 && old < p.Lp) slot_of[old] = -1;
       slot_of[pg] = v;
@@ -328,13 +357,16 @@ cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, i
   p.layer0 = layer0; p.Lp = d.Lp; p.S = d.S; p.B = d.B; p.W = d.W; p.nmax = d.nmax;
   p.N2 = ensure_sort_width(d);
   p.has_mirror = c.k_mirror != nullptr;
-  const size_t smem = (size_t)p.N2 * 12;
+  // small batches and pools: 256 threads (cheaper barriers); else 1024
+  const int threads = (p.N2 <= 1024 && d.S <= 4096) ? 256 : kEnsureThreads;
+  const bool keys_in_smem = d.S <= kSmemKeys;
+  const size_t smem = (size_t)p.N2 * 12 + (keys_in_smem ? (size_t)d.S * 4 : 0);
+  auto k = keys_in_smem ? ensure_state_kernel<true> : ensure_state_kernel<false>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(ensure_state_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = launch_pdl(ensure_state_kernel, dim3(n_layers), dim3(kEnsureThreads), smem, s, p);
+  cudaError_t e = launch_pdl(k, dim3(n_layers), dim3(threads), smem, s, p);
   count_launch();
   return e;
 }

@@ -35,61 +35,96 @@ struct ScoreParams {
   int pages_per_cta;
 };
 
-// CPL: 16-byte chunks per lane (HD = 16 * lanes * CPL).
+// Scores of this CTA's chunk of pages of request blockIdx.y, layer blockIdx.z.
+// CPL: 16-byte chunks per lane (HD = 16 * lanes * CPL).  qg: [Hkv][D] int16
+// shared memory for the group sums of q8.
 template <int CPL>
-__global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams p) {
-  extern __shared__ int16_t qg[];  // [Hkv][D] group sums of q8
-  __shared__ float red[33];
-  pdl_wait();
+__device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, int8_t* q8s,
+                                            float* red) {
   const int li = blockIdx.z, b = blockIdx.y;
   const int HD = p.Hkv * p.D;
   const int L = p.lanes;
   const int sub = threadIdx.x & (L - 1), grp = threadIdx.x / L;
   const int groups = blockDim.x / L;
-
-  // 1. issue this thread's slab loads first: they do not depend on q, so the
-  //    q quantisation below runs while they are in flight
+  const int p0 = blockIdx.x * p.pages_per_cta;
+  const int p1 = min(p.nmax, p0 + p.pages_per_cta);
   const int n_b = min(p.nmax, (p.seq_lens[b] + p.P - 1) / p.P);
-  const int p0 = blockIdx.x * p.pages_per_cta;             // pages_per_cta = groups * iters
   const int8_t* slab_l = p.slab + (size_t)(p.layer0 + li) * p.Lp * HD;
+  int32_t* out = p.scores + ((size_t)li * p.B + b) * p.nmax;
+
+  // 1. loads that depend on nothing go out first: q (16-byte vectors, the
+  //    whole [Hq][D] row of the request spread over the CTA) and the
+  //    block-table ids of the first round of pages
+  const __nv_bfloat16* qb = p.q + ((size_t)li * p.B + b) * p.Hq * p.D;
+  const int nq16 = p.Hq * p.D / 8;               // 16-byte vectors of q
+  constexpr int kQV = 4;                          // Hq * D <= 8 * 4 * 256
+  uint4 qraw[kQV];
+#pragma unroll
+  for (int j = 0; j < kQV; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    qraw[j] = i < nq16 ? reinterpret_cast<const uint4*>(qb)[i] : make_uint4(0, 0, 0, 0);
+  }
   int4 v[kScoreIters][CPL];
   bool live[kScoreIters];
+  int ids[kScoreIters];
+  auto load_ids = [&](int base) {
 #pragma unroll
-  for (int it = 0; it < kScoreIters; ++it) {
-    const int pg = p0 + it * groups + grp;
-    live[it] = false;
-    if (pg < p.nmax && pg < n_b) {
-      const int id = p.bt[(size_t)b * p.nmax + pg];
-      if (id >= 0 && id < p.Lp) {
-        live[it] = true;
-        const int4* row = reinterpret_cast<const int4*>(slab_l + (size_t)id * HD);
+    for (int it = 0; it < kScoreIters; ++it) {
+      const int pg = base + it * groups + grp;
+      ids[it] = pg < p1 ? p.bt[(size_t)b * p.nmax + pg] : -1;
+    }
+  };
+  auto load_round = [&](int base) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) v[it][c] = __ldg(row + sub + c * L);
-      } else if (sub == 0) {
-        set_status(p.status, SSA_ST_BAD_ID);
+    for (int it = 0; it < kScoreIters; ++it) {
+      const int pg = base + it * groups + grp;
+      live[it] = false;
+      if (pg < p1 && pg < n_b) {
+        const int id = ids[it];
+        if (id >= 0 && id < p.Lp) {
+          live[it] = true;
+          const int4* row = reinterpret_cast<const int4*>(slab_l + (size_t)id * HD);
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) v[it][c] = __ldg(row + sub + c * L);
+        } else if (sub == 0) {
+          set_status(p.status, SSA_ST_BAD_ID);
+        }
       }
     }
-  }
+  };
+  load_ids(p0);
+  load_round(p0);
 
-  // 2. q -> int8 with one symmetric scale per request (all heads), then the
-  //    G query heads of each KV head summed: |sum| <= 127 * G fits int16
-  const __nv_bfloat16* qb = p.q + ((size_t)li * p.B + b) * p.Hq * p.D;
+  // 2. q -> int8 with one symmetric scale per request (all heads), staged in
+  //    shared memory; then the G query heads of each KV head summed
+  //    (|sum| <= 127 * G fits int16)
+  auto lane8 = [](const uint4& u, int i) -> float {
+    const uint32_t w = i < 2 ? u.x : (i < 4 ? u.y : (i < 6 ? u.z : u.w));
+    return __uint_as_float((i & 1 ? (w >> 16) : (w & 0xFFFFu)) << 16);
+  };
   float amax = 0.0f;
-  for (int i = threadIdx.x; i < p.Hq * p.D; i += blockDim.x)
-    amax = fmaxf(amax, fabsf(__bfloat162float(qb[i])));
+#pragma unroll
+  for (int j = 0; j < kQV; ++j)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(lane8(qraw[j], i)));
   amax = block_max(amax, red);
   const float s = amax / 127.0f;
+#pragma unroll
+  for (int j = 0; j < kQV; ++j) {
+    const int vi = threadIdx.x + j * blockDim.x;
+    if (vi >= nq16) continue;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int c = 0;
+      if (amax > 0.0f) c = (int)fminf(fmaxf(rintf(lane8(qraw[j], i) / s), -127.0f), 127.0f);
+      q8s[vi * 8 + i] = (int8_t)c;
+    }
+  }
+  __syncthreads();
   for (int e = threadIdx.x; e < HD; e += blockDim.x) {
     const int h = e / p.D, d = e - h * p.D;
     int acc = 0;
-    for (int g = 0; g < p.G; ++g) {
-      int c = 0;
-      if (amax > 0.0f) {
-        float r = rintf(__bfloat162float(qb[(h * p.G + g) * p.D + d]) / s);
-        c = (int)fminf(fmaxf(r, -127.0f), 127.0f);
-      }
-      acc += c;
-    }
+    for (int g = 0; g < p.G; ++g) acc += q8s[(h * p.G + g) * p.D + d];
     qg[e] = (int16_t)acc;
   }
   __syncthreads();
@@ -101,36 +136,46 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams 
     for (int i = 0; i < 8; ++i) qa[c][i] = q2[i];
   }
 
-  // 3. exact int32 dot products, reduced over the lanes of each page
-  int32_t* out = p.scores + ((size_t)li * p.B + b) * p.nmax;
+  // 3. exact int32 dot products, reduced over the lanes of each page; the
+  //    CTA walks its pages in rounds of kScoreIters groups
+  for (int base = p0;;) {
 #pragma unroll
-  for (int it = 0; it < kScoreIters; ++it) {
-    const int pg = p0 + it * groups + grp;
-    int acc = 0;
-    if (live[it]) {
+    for (int it = 0; it < kScoreIters; ++it) {
+      const int pg = base + it * groups + grp;
+      int acc = 0;
+      if (live[it]) {
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        const int w[4] = {v[it][c].x, v[it][c].y, v[it][c].z, v[it][c].w};
+        for (int c = 0; c < CPL; ++c) {
+          const int w[4] = {v[it][c].x, v[it][c].y, v[it][c].z, v[it][c].w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc = __dp2a_lo(qa[c][2 * j], w[j], acc);
-          acc = __dp2a_hi(qa[c][2 * j + 1], w[j], acc);
+          for (int j = 0; j < 4; ++j) {
+            acc = __dp2a_lo(qa[c][2 * j], w[j], acc);
+            acc = __dp2a_hi(qa[c][2 * j + 1], w[j], acc);
+          }
         }
       }
+      for (int o = L >> 1; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (sub == 0 && pg < p1) out[pg] = live[it] ? acc : INT_MIN;
     }
-    for (int o = L >> 1; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (sub == 0 && pg < p.nmax) out[pg] = live[it] ? acc : INT_MIN;
+    base += groups * kScoreIters;
+    if (base >= p1) break;
+    load_ids(base);
+    load_round(base);
   }
 }
 
-// Histogram increment with one atomic per distinct bin per warp (keys often
-// share their top digits, which would serialise plain atomics).  Every lane
-// of the warp must call it; lanes with use == false add nothing.
-__device__ __forceinline__ void hist_add_warp(int* hist, bool use, int bin) {
-  const int lane = threadIdx.x & 31;
-  const int key = use ? bin : -1 - lane;
-  const unsigned peers = __match_any_sync(0xffffffffu, key);
-  if (use && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+// Shared memory of the score phase: qg [Hkv*D] int16, then q8s [Hq*D] int8.
+__host__ __device__ inline int qg_bytes(int HD) { return (HD * 2 + 15) / 16 * 16; }
+__host__ __device__ inline int q8_bytes(int HqD) { return (HqD + 15) / 16 * 16; }
+
+template <int CPL>
+__global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  int16_t* qg = reinterpret_cast<int16_t*>(smem_raw);
+  int8_t* q8s = reinterpret_cast<int8_t*>(smem_raw + qg_bytes(p.Hkv * p.D));
+  __shared__ float red[33];
+  pdl_wait();
+  score_chunk<CPL>(p, qg, q8s, red);
 }
 
 // ---------------------------------------------------------------------------
@@ -147,39 +192,56 @@ struct SelectParams {
   int B, nmax, P, k, W;
 };
 
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(SelectParams p) {
-  extern __shared__ uint32_t key[];      // [nmax] order-preserving score keys
+// Top-k selection of one (layer, request) row of scores by the whole CTA.
+// CG: the row was written by other CTAs of this kernel (read past L1).
+template <bool CG>
+__device__ void select_row(const int32_t* row, int n, int k, int W, int32_t* out,
+                           int32_t* n_sel_out, int32_t* status, uint32_t* key) {
   __shared__ int hist[256];
   __shared__ int tmp[33];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_remaining;
-  pdl_wait();
-  const int b = blockIdx.x, li = blockIdx.y;
+  __shared__ uint32_t s_lo, s_hi, s_base;
+  __shared__ int s_remaining, s_shift;
   const int tid = threadIdx.x, nt = blockDim.x;
-  const int n = min(p.nmax, (p.seq_lens[b] + p.P - 1) / p.P);
-  const int32_t* row = p.scores + ((size_t)li * p.B + b) * p.nmax;
-  int32_t* out = p.sel + ((size_t)li * p.B + b) * p.W;
-
-  const bool take_all = (n - 1 <= p.k);
+  const bool take_all = (n - 1 <= k);
   const int cand = n - 1;                // pages that compete; n-1 is forced
   uint32_t T = 0;
   int need_eq = 0;
   if (!take_all) {
-    for (int i = tid; i < cand; i += nt) key[i] = (uint32_t)row[i] ^ 0x80000000u;
-    if (tid == 0) { s_prefix = 0; s_remaining = p.k; }
-    uint32_t mask = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    // order-preserving keys and their range
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int i = tid; i < cand; i += nt) {
+      const uint32_t kk = (uint32_t)(CG ? __ldcg(row + i) : row[i]) ^ 0x80000000u;
+      key[i] = kk;
+      lo = min(lo, kk);
+      hi = max(hi, kk);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (tid == 0) { s_lo = 0xFFFFFFFFu; s_hi = 0u; s_remaining = k; }
+    __syncthreads();
+    if ((tid & 31) == 0) { atomicMin(&s_lo, lo); atomicMax(&s_hi, hi); }
+    __syncthreads();
+    // MSB-first radix search for the k-th largest key, restricted to the
+    // keys' own range [lo, hi]: bins of 8 bits of (key - lo), starting at the
+    // highest bit the range uses, so a narrow range needs fewer passes
+    uint32_t base = s_lo;                 // keys below base are out
+    const uint32_t range = s_hi - s_lo;
+    int shift = range == 0 ? 0 : max(0, 32 - __clz((int)range) - 8);
+    if (range >> 31) shift = 24;
+    uint32_t span_hi = s_hi;              // candidates lie in [base, span_hi]
+    for (;;) {
       for (int i = tid; i < 256; i += nt) hist[i] = 0;
       __syncthreads();
-      const uint32_t prefix = s_prefix;
-      for (int base = 0; base < cand; base += nt) {       // uniform trip count
-        const int i = base + tid;
-        const uint32_t kk = i < cand ? key[i] : 0u;
-        hist_add_warp(hist, i < cand && (kk & mask) == prefix, (int)((kk >> shift) & 255));
+      for (int i = tid; i < cand; i += nt) {
+        const uint32_t kk = key[i];
+        if (kk >= base && kk <= span_hi) atomicAdd(&hist[((kk - base) >> shift) & 255], 1);
       }
       __syncthreads();
       if (tid < 32) {
-        // lane l covers digits 255-8l down to 248-8l (largest first)
+        // lane l covers bins 255-8l down to 248-8l (largest first)
         int cnt[8], sum = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) { cnt[j] = hist[255 - 8 * tid - j]; sum += cnt[j]; }
@@ -190,71 +252,138 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(SelectParams p
           if (tid >= o) incl += y;
         }
         const int rem = s_remaining;
-        const unsigned hit = __ballot_sync(0xffffffffu, incl >= rem);
-        const int lane = __ffs(hit) - 1;       // hit != 0: rem <= total
+        const unsigned hitm = __ballot_sync(0xffffffffu, incl >= rem);
+        const int lane = __ffs(hitm) - 1;       // hitm != 0: rem <= candidates
         if (tid == lane) {
           int above = incl - sum;
           for (int j = 0; j < 8; ++j) {
             if (above + cnt[j] >= rem) {
+              const uint32_t bin = (uint32_t)(255 - 8 * tid - j);
               s_remaining = rem - above;
-              s_prefix = prefix | ((uint32_t)(255 - 8 * tid - j) << shift);
+              s_base = base + (bin << shift);
+              s_shift = shift;
               break;
             }
             above += cnt[j];
           }
         }
       }
-      mask |= 0xFFu << shift;
       __syncthreads();
+      base = s_base;
+      if (shift == 0) break;
+      span_hi = (uint32_t)min((unsigned long long)base + ((1ull << shift) - 1ull),
+                              0xFFFFFFFFull);
+      shift = shift >= 8 ? shift - 8 : 0;
     }
-    T = s_prefix;
-    need_eq = s_remaining;
+    T = base;                             // the k-th largest key
+    need_eq = s_remaining;                // how many keys equal to T to take
   }
 
-  // ranks in page order: contiguous runs of pages per thread
+  // Ordered compaction, one packed scan.  Each page is "above" (forced, or
+  // key > T: always taken), "equal" (key == T: the first need_eq in page
+  // order are taken) or out.  A taken page's output slot is the number of
+  // above pages before it plus min(equal pages before it, need_eq).
   const int per = (n + nt - 1) / nt;
   const int a0 = min(n, tid * per), a1 = min(n, a0 + per);
-  int eq_before = 0;
-  if (!take_all) {
-    int eq = 0;
-    for (int i = a0; i < a1; ++i) eq += (i < cand && key[i] == T);
-    int tot;
-    eq_before = block_exclusive_scan(eq, tmp, tot);
+  auto kind = [&](int i) -> int {          // 2 above, 1 equal, 0 out
+    if (take_all || i == cand) return 2;
+    const uint32_t kk = key[i];
+    return kk > T ? 2 : (kk == T ? 1 : 0);
+  };
+  int gt = 0, eq = 0;
+  for (int i = a0; i < a1; ++i) {
+    const int t = kind(i);
+    gt += t == 2;
+    eq += t == 1;
   }
-  int mine = 0;
-  {
-    int e = eq_before;
-    for (int i = a0; i < a1; ++i) {
-      bool f;
-      if (take_all || i == cand) f = true;
-      else if (key[i] > T) f = true;
-      else if (key[i] == T) f = (e++ < need_eq);
-      else f = false;
-      mine += f;
-    }
-  }
-  int total;
-  int off = block_exclusive_scan(mine, tmp, total);
-  {
-    int e = eq_before;
-    for (int i = a0; i < a1; ++i) {
-      bool f;
-      if (take_all || i == cand) f = true;
-      else if (key[i] > T) f = true;
-      else if (key[i] == T) f = (e++ < need_eq);
-      else f = false;
-      if (f) {
-        if (off < p.W) out[off] = i;
-        ++off;
+  int packed_total;
+  const int packed = block_exclusive_scan((gt << 16) | eq, tmp, packed_total);
+  int g_before = packed >> 16, e_before = packed & 0xFFFF;
+  const int total = (packed_total >> 16) + min(packed_total & 0xFFFF, need_eq);
+  for (int i = a0; i < a1; ++i) {
+    const int t = kind(i);
+    if (t == 2) {
+      const int off = g_before + min(e_before, need_eq);
+      if (off < W) out[off] = i;
+      ++g_before;
+    } else if (t == 1) {
+      if (e_before < need_eq) {
+        const int off = g_before + e_before;
+        if (off < W) out[off] = i;
       }
+      ++e_before;
     }
   }
-  const int kept = min(total, p.W);
-  for (int i = kept + tid; i < p.W; i += nt) out[i] = -1;
+  const int kept = min(total, W);
+  for (int i = kept + tid; i < W; i += nt) out[i] = -1;
   if (tid == 0) {
-    p.n_sel[(size_t)li * p.B + b] = kept;
-    if (total > p.W) set_status(p.status, SSA_ST_DROP);
+    *n_sel_out = kept;
+    if (total > W) set_status(status, SSA_ST_DROP);
   }
+}
+
+__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(SelectParams p) {
+  extern __shared__ uint32_t key[];      // [nmax] order-preserving score keys
+  pdl_wait();
+  const int b = blockIdx.x, li = blockIdx.y;
+  const int n = min(p.nmax, (p.seq_lens[b] + p.P - 1) / p.P);
+  select_row<false>(p.scores + ((size_t)li * p.B + b) * p.nmax, n, p.k, p.W,
+                    p.sel + ((size_t)li * p.B + b) * p.W, p.n_sel + (size_t)li * p.B + b,
+                    p.status, key);
+}
+
+// a1 + a2 in one launch: every CTA scores its chunk of pages; the last CTA of
+// each (layer, request) to finish -- an atomic ticket, no CTA waits for
+// another -- selects over the whole row.
+struct FusedParams {
+  ScoreParams s;
+  int32_t* sel;          // [n_layers][B][W]
+  int32_t* n_sel;        // [n_layers][B]
+  int32_t* tickets;      // [n_layers][B], zero between calls
+  int k, W, qg_bytes;
+};
+
+template <int CPL>
+__global__ void __launch_bounds__(kScoreThreads) index_topk_kernel(FusedParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  int16_t* qg = reinterpret_cast<int16_t*>(smem_raw);
+  int8_t* q8s = reinterpret_cast<int8_t*>(smem_raw + qg_bytes(p.s.Hkv * p.s.D));
+  uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw + p.qg_bytes);   // [nmax]
+  __shared__ float red[33];
+  __shared__ int s_last;
+  pdl_wait();
+  score_chunk<CPL>(p.s, qg, q8s, red);
+  const int b = blockIdx.y, li = blockIdx.z;
+  const size_t rb = (size_t)li * p.s.B + b;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&p.tickets[rb], 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int n = min(p.s.nmax, (p.s.seq_lens[b] + p.s.P - 1) / p.s.P);
+  select_row<true>(p.s.scores + rb * p.s.nmax, n, p.k, p.W, p.sel + rb * p.W, p.n_sel + rb,
+                   p.s.status, key);
+  if (threadIdx.x == 0) p.tickets[rb] = 0;      // ready for the next call
+}
+
+// Pages per score CTA: the smallest multiple of one round (kScoreIters page
+// groups) that keeps the grid within one wave of resident CTAs (occ per SM),
+// so no CTA waits for a second wave.
+int score_pages_per_cta(const Dims& d, int n_layers, int lanes, int occ) {
+  const int round = kScoreIters * (kScoreThreads / lanes);
+  int sms = 152;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 152;
+  if (occ < 1) occ = 1;
+  const long long rows = (long long)d.B * n_layers;
+  long long chunks = (long long)sms * occ / rows;
+  if (chunks < 1) chunks = 1;
+  long long per = (d.nmax + chunks - 1) / chunks;
+  per = (per + round - 1) / round * round;
+  return (int)per;
 }
 
 }  // namespace
@@ -275,11 +404,63 @@ cudaError_t launch_index_scores(const Dims& d, const ssa_cache& c, int layer0, i
   const int chunks16 = d.Hkv * d.D / 16;       // 16-byte chunks per page row
   const int cpl = chunks16 > 32 ? 2 : 1;
   p.lanes = chunks16 / cpl;
-  p.pages_per_cta = kScoreIters * (kScoreThreads / p.lanes);
+  const size_t smem = (size_t)qg_bytes(d.Hkv * d.D) + q8_bytes(d.Hq * d.D);
+  int occ = 1;
+  cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &occ, cpl == 1 ? index_score_kernel<1> : index_score_kernel<2>, kScoreThreads, smem);
+  if (oe != cudaSuccess) return oe;
+  p.pages_per_cta = score_pages_per_cta(d, n_layers, p.lanes, occ);
   dim3 grid((d.nmax + p.pages_per_cta - 1) / p.pages_per_cta, d.B, n_layers);
-  const size_t smem = (size_t)d.Hkv * d.D * sizeof(int16_t);
   cudaError_t e = cpl == 1 ? launch_pdl(index_score_kernel<1>, grid, dim3(kScoreThreads), smem, s, p)
                            : launch_pdl(index_score_kernel<2>, grid, dim3(kScoreThreads), smem, s, p);
+  count_launch();
+  return e;
+}
+
+cudaError_t launch_index_topk(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                              const void* q, const int32_t* bt, const int32_t* seq_lens,
+                              int32_t* scores, int32_t* sel, int32_t* n_sel, int32_t* tickets,
+                              int32_t* status, cudaStream_t s) {
+  FusedParams f{};
+  ScoreParams& p = f.s;
+  p.slab = c.slab;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.bt = bt;
+  p.seq_lens = seq_lens;
+  p.scores = scores;
+  p.status = status;
+  p.layer0 = layer0;
+  p.Lp = d.Lp; p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.G = d.G; p.D = d.D; p.P = d.P;
+  p.nmax = d.nmax;
+  const int chunks16 = d.Hkv * d.D / 16;
+  const int cpl = chunks16 > 32 ? 2 : 1;
+  p.lanes = chunks16 / cpl;
+  f.sel = sel;
+  f.n_sel = n_sel;
+  f.tickets = tickets;
+  f.k = d.k;
+  f.W = d.W;
+  f.qg_bytes = qg_bytes(d.Hkv * d.D) + q8_bytes(d.Hq * d.D);     // key[] after qg, q8s
+  const size_t smem = (size_t)f.qg_bytes + (size_t)d.nmax * sizeof(uint32_t);
+  int occ = 1;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &occ, cpl == 1 ? index_topk_kernel<1> : index_topk_kernel<2>, kScoreThreads, smem);
+  if (e != cudaSuccess) return e;
+  p.pages_per_cta = score_pages_per_cta(d, n_layers, p.lanes, occ);
+  dim3 grid((d.nmax + p.pages_per_cta - 1) / p.pages_per_cta, d.B, n_layers);
+  if (cpl == 1) {
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(index_topk_kernel<1>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+      return e;
+    e = launch_pdl(index_topk_kernel<1>, grid, dim3(kScoreThreads), smem, s, f);
+  } else {
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(index_topk_kernel<2>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+      return e;
+    e = launch_pdl(index_topk_kernel<2>, grid, dim3(kScoreThreads), smem, s, f);
+  }
   count_launch();
   return e;
 }

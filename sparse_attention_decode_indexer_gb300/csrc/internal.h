@@ -34,6 +34,11 @@ cudaError_t launch_store(const Dims& d, const ssa_cache& c, int layer0, int n_la
 cudaError_t launch_index_scores(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
                                 const void* q, const int32_t* bt, const int32_t* seq_lens,
                                 int32_t* scores, int32_t* status, cudaStream_t s);
+// a1 + a2 fused: scores, then the last CTA per (layer, request) selects.
+cudaError_t launch_index_topk(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                              const void* q, const int32_t* bt, const int32_t* seq_lens,
+                              int32_t* scores, int32_t* sel, int32_t* n_sel, int32_t* tickets,
+                              int32_t* status, cudaStream_t s);
 cudaError_t launch_topk_select(const Dims& d, int n_layers, const int32_t* scores,
                                const int32_t* seq_lens, int32_t* sel, int32_t* n_sel,
                                int32_t* status, cudaStream_t s);

@@ -1,0 +1,48 @@
+"""GPU parity at the full sizes of the synthetic workloads, in the benchmark's
+launch configuration: the library runs every layer in one launch per stage;
+the oracle (which finishes a layer in seconds) checks sampled layers after
+every decode step of the query walk.  Bit-exact selection, remap, miss lists
+and LRU state each step; pool bytes at the end; outputs within tolerance.
+"""
+import pytest
+
+import workloads as wl
+from tests.parity import run_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def test_batched_32k_bf16_needles_full():
+    w = wl.WORKLOADS["batched_32k_bf16_needles"]
+    rep = {}
+    run, orc = run_parity(w, oracle_layers=[0, 11], pool_every_step=False, report=rep)
+    pages = wl.needle_pages(w)
+    for l in (0, 11):
+        sel = run.sel[l].cpu().numpy()
+        for b in range(w.batch):
+            assert set(pages[b].tolist()) <= set(sel[b].tolist())
+    print(w.name, rep)
+
+
+def test_lru_pressure_64k_fp8_full():
+    w = wl.WORKLOADS["lru_pressure_64k_fp8"]
+    rep = {}
+    run_parity(w, oracle_layers=[0, 7], pool_every_step=False, check_mirror=True, report=rep)
+    assert rep["misses"] > 0
+    print(w.name, rep)
+
+
+def test_host_tier_196k_fp8_full():
+    w = wl.WORKLOADS["host_tier_196k_fp8"]
+    rep = {}
+    run_parity(w, oracle_layers=[5], pool_every_step=False, report=rep)
+    assert rep["misses"] > 0
+    print(w.name, rep)
+
+
+@pytest.mark.parametrize("fp8,frac", [(False, 1.0), (True, 0.2)], ids=["bf16_resident", "fp8_20pct"])
+def test_sweep_128k_batch1_full(fp8, frac):
+    w = wl.sweep_workload(1, fp8, frac, steps=6)
+    rep = {}
+    run_parity(w, oracle_layers=[3], pool_every_step=False, report=rep)
+    print(w.name, rep)

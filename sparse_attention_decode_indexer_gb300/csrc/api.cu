@@ -95,12 +95,7 @@ struct WsLayout {
 };
 
 size_t part_entries(const Dims& d) {
-  size_t best = 0;
-  for (int nl = 1; nl <= d.Lyr; ++nl) {
-    const size_t e = (size_t)nl * d.B * d.Hkv * decode_splits(d, nl, num_sms());
-    if (e > best) best = e;
-  }
-  return best * d.G;
+  return (size_t)decode_max_ctas(d, num_sms()) * 2 * d.G;
 }
 
 WsLayout ws_layout(const Dims& d) {
@@ -239,24 +234,23 @@ int ssa_sparse_paged_decode(const ssa_layout* lay, const ssa_cache* c, int layer
     return SSA_ERR_INVALID_ARG;
   if ((r = check_range(d, layer0, n_layers))) return r;
   if (!q || !sel || !phys || !seq_lens || !out) return SSA_ERR_INVALID_ARG;
-  const int splits = decode_splits(d, n_layers, num_sms());
-  if (splits > 1 && !ws) return SSA_ERR_INVALID_ARG;
+  if (!ws) return SSA_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(d);
   DecodeArgs a{};
   a.d = &d;
   a.c = c;
   a.layer0 = layer0;
   a.n_layers = n_layers;
-  a.splits = splits;
+  a.num_sms = num_sms();
   a.q = q;
   a.sel = sel;
   a.phys = phys;
   a.seq_lens = seq_lens;
   a.sm_scale = sm_scale;
   a.out = out;
-  a.part_o = ws ? at<float>(ws, w.part_o) : nullptr;
-  a.part_ml = ws ? at<float>(ws, w.part_ml) : nullptr;
-  a.tickets = ws ? at<int32_t>(ws, w.tickets) : nullptr;
+  a.part_o = at<float>(ws, w.part_o);
+  a.part_ml = at<float>(ws, w.part_ml);
+  a.tickets = at<int32_t>(ws, w.tickets);
   a.status = status;
   cudaError_t e = launch_decode(a, (cudaStream_t)stream);
   return e == cudaSuccess ? SSA_OK : fail_cuda(e);

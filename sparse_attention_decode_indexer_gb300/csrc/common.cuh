@@ -107,6 +107,12 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Bring the line holding a global address into L2 (no data returned, so it
+// cannot race with writers; it also walks the address translation).
+__device__ __forceinline__ void prefetch_l2(const void* gptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(gptr));
+}
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch: every kernel of the library is launched so
 // that it may start while the previous kernel on the stream drains, and
@@ -114,6 +120,14 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 // no-op when the kernel was launched without the attribute.)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel on the stream be scheduled now: its CTAs run their
+// set-up while this grid drains, then block in pdl_wait() until this grid
+// has completed and its writes are visible.  Where the trigger sits decides
+// only when the next grid may start, never what it reads.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -164,12 +178,40 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four floats -> four e4m3 codes (round to nearest even, saturating), x[0]
+// in byte 0.
+__device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
 // Four e4m3 codes (one 32-bit word) -> two f16x2: lo = bytes 0,1; hi = bytes
 // 2,3.  Exact: every e4m3 value is an f16 value.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %2;\n"
       "cvt.rn.f16x2.e4m3x2 %0, l;\ncvt.rn.f16x2.e4m3x2 %1, h;\n}"
       : "=r"(lo), "=r"(hi) : "r"(w));
+}
+
+// Four e4m3 codes -> their four values as floats (exact).
+__device__ __forceinline__ void e4m3x4_to_f32x4(uint32_t w, float& x0, float& x1, float& x2,
+                                                float& x3) {
+  uint32_t lo, hi;
+  e4m3x4_to_f16x2x2(w, lo, hi);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  x0 = a.x; x1 = a.y; x2 = b.x; x3 = b.y;
 }
 
 // 2^x, hardware approximation (ex2.approx; ~2 ulp, flushes subnormals).

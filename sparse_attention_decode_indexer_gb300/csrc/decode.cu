@@ -8,14 +8,28 @@
 // V = code * v_scale[t]).
 //
 // Design (sm_103a):
-//   * grid (split, b*Hkv+h, layer); each CTA takes a contiguous share of the
-//     valid selected pages of its (layer, request, KV head);
-//   * one producer warp streams each page's K and V (one KV head, P tokens)
-//     into shared memory with TMA tiled copies (128-byte swizzle), plus the
-//     fp8 per-token scales with bulk copies, through an mbarrier ring;
-//   * four consumer warps each take 16-token blocks: QK^T and PV as
-//     m16n8k16 tensor-core tiles with the G <= 8 query heads as the M rows,
-//     fp32 accumulate, online softmax in the log2 domain with warp shuffles;
+//   * work partition: a "unit" is one (layer, request, KV head); each unit
+//     weighs w = min(n_max, k + 1) tiles (the selection size of a request
+//     with at least k + 1 pages).  The units' tiles form one line of
+//     T = units * w tiles that a single wave of CTAs cuts into equal
+//     contiguous ranges, so every SM streams the same number of pages
+//     whatever the unit count.  A CTA's range holds whole units and at most
+//     two pieces of units it shares with its neighbours; a piece maps its
+//     share of the unit's weight onto the same share of the unit's valid
+//     selected pages;
+//   * one producer warp walks the range: per unit it reads the sel/phys row,
+//     counts the valid entries and streams its piece's pages (one KV head,
+//     P tokens of K and V) into shared memory with TMA tiled copies (128-byte
+//     swizzle), plus the fp8 per-token scales with bulk copies, through an
+//     mbarrier ring.  Each stage carries a small descriptor (first/last page
+//     of a piece, valid tokens, unit); the first page of a piece also brings
+//     the unit's G query rows.  Empty pieces and the end of the range travel
+//     as stages without data;
+//   * four consumer warps each take 16-token blocks: QK^T with the tokens as
+//     the MMA rows (A = K, B = q^T, N = 8 query heads) and PV with d as the
+//     rows (A = V^T, B = P^T, the probabilities transposed in registers by
+//     movmatrix), m16n8k16 tensor-core tiles, fp32 accumulate, online softmax
+//     in the log2 domain with warp shuffles;
 //   * bf16 K/V: bf16 MMAs, ldmatrix (V transposed by ldmatrix.trans);
 //   * fp8 K/V: the e4m3 codes convert exactly to f16, so the MMAs run in f16
 //     on the raw codes; q is scaled by a power of two into f16 range, the K
@@ -24,12 +38,17 @@
 //     f16 operand never overflows).  V is stored d-major in the pool
 //     ([Hkv][D][P]) so that the 8-bit reads run along tokens, the reduction
 //     axis of PV;
-//   * the 4 warps' states merge in shared memory; with several splits the
-//     CTA writes (m, l, o) partials and a merge kernel combines them.
+//   * at the end of a piece each consumer warp leaves its softmax state in
+//     shared memory and streams on; a sixth warp combines the 4 states: a
+//     whole unit becomes its output, a shared unit's piece an (m, l, o)
+//     partial that it publishes (GPU-scope fence, atomic ticket); the last
+//     piece of a unit to arrive merges the unit's partials into the output.
+//     No CTA ever waits for another, no consumer warp for another.
 // The work is HBM-bound (8 flop/byte bf16, 16 fp8): the tensor cores carry
 // the G-row tiles, the memory system sets the pace.
 #include <cudaTypedefs.h>
 #include <cuda.h>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 
@@ -41,8 +60,23 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kConsumerWarps = 4;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kMergeWarp = kConsumerWarps + 1;
+constexpr int kDecodeThreads = kConsumers + 64;
 constexpr int kMaxG = 8;
+constexpr int kWindow = 32;          // producer compaction window (entries)
+constexpr int kMaxStages = 12;
+constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kSmemPerCtaMax = 227 * 1024;
+constexpr int kSmemReservedPerCta = 1024;
+
+// stage descriptor flags
+constexpr int kFirst = 1;   // first page of a piece: the stage also holds q
+constexpr int kLast = 2;    // last page of a piece: flush after it
+constexpr int kEmpty = 4;   // a piece without pages (no data in the stage)
+constexpr int kDone = 8;    // end of the CTA's range
+constexpr int kFinal = 16;  // with kLast / kEmpty: the CTA's last piece
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -50,13 +84,23 @@ template <bool FP8, int P>
 struct Cfg {
   static constexpr int kTileBytes = P * kD * (FP8 ? 1 : 2);      // one KV head of one page
   static constexpr int kScaleBytes = FP8 ? 2 * P * 4 : 0;
-  static constexpr int kStageBytes = round_up(2 * kTileBytes + kScaleBytes, 1024);
-  static constexpr int kStages = FP8 ? 4 : 3;
+  static constexpr int kQOff = 2 * kTileBytes + kScaleBytes;
+  static constexpr int kQBytes = kMaxG * kD * 2;
+  static constexpr int kStageBytes = round_up(kQOff + kQBytes, 1024);
+  static constexpr int kCombineBytes = kConsumerWarps * kMaxG * kD * 4 + 2 * kConsumerWarps * kMaxG * 4;
+  // alignment slack, combine area, producer window, descriptors and barriers
+  static constexpr int kFixed = 1024 + kCombineBytes + kWindow * 8 + kMaxStages * 32 + 64;
+  // two CTAs per SM when at least two stages fit beside the second CTA
+  static constexpr int kStages2 = (kSmemPerSm / 2 - kSmemReservedPerCta - kFixed) / kStageBytes;
+  static constexpr int kCtasPerSm = kStages2 >= 2 ? 2 : 1;
+  static constexpr int kStagesFit =
+      kCtasPerSm == 2 ? kStages2 : (kSmemPerCtaMax - kFixed) / kStageBytes;
+  static constexpr int kStages = kStagesFit > kMaxStages ? kMaxStages : kStagesFit;
   static constexpr int kBlocks = P / 16;                          // 16-token blocks per page
   // log2 of the fp8 V^T row swizzle span in 16-byte units (row = P bytes)
   static constexpr int kVSwz = P >= 128 ? 3 : (P == 64 ? 2 : (P == 32 ? 1 : 0));
-  static_assert(kConsumerWarps * kMaxG * kD * 4 + 2 * kConsumerWarps * kMaxG * 4 <=
-                kStages * kStageBytes, "combine area must fit in the stage ring");
+  static_assert(kStages >= 2, "at least two stages");
+  static_assert(kQOff % 16 == 0, "q rows need a 16-byte aligned bulk copy");
 };
 
 struct DecodeParams {
@@ -67,11 +111,12 @@ struct DecodeParams {
   const float* k_scale;     // [Lyr][S][P]
   const float* v_scale;
   __nv_bfloat16* out;       // [n_layers][B][Hq][D]
-  float* part_o;            // [units][splits][G][D]
-  float* part_ml;           // [units][splits][G][2]
-  int32_t* tickets;         // [units] split counters, zero between calls
+  float* part_o;            // [n_ctas][2][G][D]
+  float* part_ml;           // [n_ctas][2][G][2]
+  int32_t* tickets;         // [units] piece counters, zero between calls
   int32_t* status;
-  int layer0, B, Hq, Hkv, G, W, S, splits;
+  int T, tq, tr;             // tiles (units * w); CTA c holds [c*tq + min(c, tr), ...)
+  int layer0, B, Hq, Hkv, G, W, S, w;
   float sm_log2;            // sm_scale * log2(e)
 };
 
@@ -87,18 +132,6 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-}
-
-// Producer warp -> consumer warps: the page list is written (barrier 2).
-__device__ __forceinline__ void list_publish() {
-  asm volatile("bar.arrive 2, %0;" ::"n"(kDecodeThreads) : "memory");
-}
-__device__ __forceinline__ void list_wait() {
-  asm volatile("bar.sync 2, %0;" ::"n"(kDecodeThreads) : "memory");
-}
-
 // 1/x for x a positive normal power of two, exactly, without a division.
 __device__ __forceinline__ float pow2_rcp(float x) {
   return __uint_as_float(0x7F000000u - __float_as_uint(x));
@@ -108,84 +141,245 @@ __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// |x| max of the 8 bf16 values in a 16-byte word
+__device__ __forceinline__ float bf16x8_absmax(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = fmaxf(m, __uint_as_float((w[i] << 16) & 0x7FFF0000u));
+    m = fmaxf(m, __uint_as_float(w[i] & 0x7FFF0000u));
+  }
+  return m;
+}
+
+// First tile of CTA c (the first tr CTAs hold tq + 1 tiles, the others
+// tq), and the CTA that holds tile t (the inverse).
+__device__ __forceinline__ int tile_begin(const DecodeParams& p, int c) {
+  return c * p.tq + min(c, p.tr);
+}
+__device__ __forceinline__ int cta_of(const DecodeParams& p, int t) {
+  const int big = p.tr * (p.tq + 1);
+  return t < big ? t / (p.tq + 1) : p.tr + (t - big) / p.tq;
+}
+
 template <bool FP8, int P>
-__global__ void __launch_bounds__(kDecodeThreads, FP8 ? 3 : 2)
+__global__ void __launch_bounds__(kDecodeThreads, Cfg<FP8, P>::kCtasPerSm)
 decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV) {
   using C = Cfg<FP8, P>;
   constexpr int NST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned (the TMA swizzle atom) by pointer arithmetic on the
+  // shared array itself, so that every access below stays a shared-memory
+  // access the compiler can tell apart from global memory
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem;
-  int2* plist = reinterpret_cast<int2*>(smem + NST * C::kStageBytes);     // [W]
-  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(plist + round_up(p.W, 2));  // [8][D]
-  uint64_t* full = reinterpret_cast<uint64_t*>(qs + kMaxG * kD);
+  float* comb = reinterpret_cast<float*>(smem + NST * C::kStageBytes);
+  int2* plist = reinterpret_cast<int2*>(smem + NST * C::kStageBytes + C::kCombineBytes);
+  int4* meta = reinterpret_cast<int4*>(plist + kWindow);                  // [NST]
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + NST);
   uint64_t* empty = full + NST;
-  __shared__ int s_nv;
+  uint64_t* cfull = empty + NST;           // the consumers' states are in comb
+  uint64_t* cfree = cfull + 1;             // the merge warp is done reading comb
+  uint64_t* cbar = cfree + 1;              // the consumer warps' barrier (last piece)
   __shared__ int s_abort;
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, bh = blockIdx.y, li = blockIdx.z;
-  const int b = bh / p.Hkv, h = bh - b * p.Hkv;
-  const int layer = p.layer0 + li;
+  const int cta = blockIdx.x;
 
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
+    mbar_init(cfull, kConsumerWarps);
+    mbar_init(cfree, 1);
+    mbar_init(cbar, kConsumerWarps);
     s_abort = 0;
     fence_barrier_init();
   }
-  __syncthreads();
-  pdl_wait();                 // sel, phys, q and the pool come from earlier kernels
-  const int seq_len = p.seq_lens[b];
-
-  if (warp == kConsumerWarps) {
-    // ---------------- producer warp: the page list, then one elected thread
-    // issues every copy (the consumers meanwhile stage q) ----------------
+  // the CTA's range, from the launch parameters alone: computed (and the
+  // pages it will touch prefetched into L2, which also walks their address
+  // translations) while the previous kernel drains
+  const int t0 = tile_begin(p, cta), t1 = tile_begin(p, cta + 1);
+  const int u_first = t0 / p.w, u_last = (t1 - 1) / p.w;
+  if (warp == kProducerWarp) {
     if (lane == 0) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
     }
-    const int32_t* selr = p.sel + ((size_t)li * p.B + b) * p.W;
-    const int32_t* physr = p.phys + ((size_t)li * p.B + b) * p.W;
-    int cnt = 0;
-    for (int base = 0; base < p.W; base += 32) {
-      const int i = base + lane;
-      int pg = -1, sl = -1;
-      if (i < p.W) { pg = selr[i]; sl = physr[i]; }
-      const bool ok = pg >= 0 && sl >= 0 && sl < p.S;
-      if (pg >= 0 && sl < 0) set_status(p.status, SSA_ST_UNRESOLVED);
-      if (pg >= 0 && sl >= p.S) set_status(p.status, SSA_ST_BAD_ID);
-      const unsigned m = __ballot_sync(0xffffffffu, ok);
-      if (ok) plist[cnt + __popc(m & ((1u << lane) - 1u))] = make_int2(pg, sl);
-      cnt += __popc(m);
-    }
-    if (lane == 0) s_nv = cnt;
-    list_publish();           // page list and count visible to the consumers
-    const int i0 = (int)((long long)cnt * split / p.splits);
-    const int nst = (int)((long long)cnt * (split + 1) / p.splits) - i0;
-    if (lane != 0 || nst <= 0) return;
-    int issued = 0;
-    bool aborted = false;
-    for (int st = 0; st < nst; ++st) {
-      const int sb = st % NST;
-      if (st >= NST && !mbar_wait(&empty[sb], ((st / NST) - 1) & 1, &s_abort)) {
-        aborted = true;
-        break;
+    const int row = u_first / p.Hkv;
+    const void* pf = lane == 0   ? (const void*)(p.sel + (size_t)row * p.W)
+                     : lane == 1 ? (const void*)(p.phys + (size_t)row * p.W)
+                     : lane == 2 ? (const void*)(p.seq_lens + row % p.B)
+                     : lane == 3 ? (const void*)(p.q + (size_t)u_first * p.G * kD)
+                     : lane == 4 ? (const void*)(p.out + (size_t)u_first * p.G * kD)
+                     : lane == 5 ? (const void*)(p.part_o + (size_t)cta * 2 * p.G * kD)
+                     : lane == 6 ? (const void*)(p.part_ml + (size_t)cta * 2 * p.G * 2)
+                                 : (const void*)(p.tickets + u_first);
+    if (lane < 8) prefetch_l2(pf);
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();                 // sel, phys, q and the pool come from earlier kernels
+
+  if (warp == kMergeWarp) {
+    // ---------------- merge warp ---------------------------------------------
+    // At the end of each piece but the CTA's last the consumers leave their
+    // 4 softmax states in comb and stream on; this warp combines them: a
+    // whole unit becomes its output, a shared unit's piece an (m, l, o)
+    // partial, which it publishes (GPU-scope fence, atomic ticket).  The
+    // last piece of a unit to arrive merges every piece into the output (a7).
+    // The consumers finish the CTA's last piece themselves.
+    const float* cO = comb;                                      // [4][8][D]
+    const float* cM = cO + kConsumerWarps * kMaxG * kD;           // [4][8]
+    const float* cL = cM + kConsumerWarps * kMaxG;                // [4][8]
+    const int wl = lane >> 3, gl = lane & 7;      // lane = (warp, head) of the weights
+    for (int u = u_first, k = 0; u < u_last; ++u, ++k) {
+      if (!mbar_wait(cfull, k & 1, &s_abort)) {
+        if (lane == 0) set_status(p.status, SSA_ST_TIMEOUT);
+        return;
       }
-      const int2 e = plist[i0 + st];
-      const int row_k = ((layer * p.S + e.y) * p.Hkv + h) * P;
+      const int us = u * p.w;
+      const int c_first = cta_of(p, us), c_last = cta_of(p, us + p.w - 1);
+      const bool whole = c_first == c_last;
+      const size_t pslot = (size_t)cta * 2 + (t0 >= us ? 0 : 1);
+      // per head: M = max over the warps, the warps' factors, L
+      const float mw = cM[wl * kMaxG + gl];
+      float M = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 8));
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+      const float f = M == -INFINITY ? 0.0f : fast_exp2(mw - M);
+      float L = cL[wl * kMaxG + gl] * f;
+      L += __shfl_xor_sync(0xffffffffu, L, 8);
+      L += __shfl_xor_sync(0xffffffffu, L, 16);
+      __nv_bfloat16* outu = p.out + (size_t)u * p.G * kD;
+#pragma unroll
+      for (int gg = 0; gg < kMaxG; ++gg) {
+        float fw[kConsumerWarps];
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) fw[w] = __shfl_sync(0xffffffffu, f, w * kMaxG + gg);
+        const float Mg = __shfl_sync(0xffffffffu, M, gg), Lg = __shfl_sync(0xffffffffu, L, gg);
+        if (gg >= p.G) continue;
+        const float rL = Lg > 0.0f ? 1.0f / Lg : 0.0f;
+#pragma unroll
+        for (int i = 0; i < kD / 32; ++i) {
+          const int d = lane + 32 * i, dz = d ^ (8 * ((gg >> 1) & 3));
+          float O = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) O += cO[(w * kMaxG + gg) * kD + dz] * fw[w];
+          if (whole) outu[gg * kD + d] = __float2bfloat16_rn(O * rL);
+          else p.part_o[(pslot * p.G + gg) * kD + d] = O;
+        }
+        if (!whole && lane == 0) {
+          p.part_ml[(pslot * p.G + gg) * 2] = Mg;
+          p.part_ml[(pslot * p.G + gg) * 2 + 1] = Lg;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cfree);     // comb may take the next piece
+      if (whole) continue;
+      int last = 0;
+      if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(&p.tickets[u], 1) == c_last - c_first;
+      }
+      if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+      __threadfence();
+      const int np = c_last - c_first + 1;
+      const int slot0 = tile_begin(p, c_first) == us ? 0 : 1;
+      // pieces: (c_first, slot0), then (c, 0) for c_first < c <= c_last
+      auto piece = [&](int kk) -> size_t {
+        return ((size_t)(c_first + kk) * 2 + (kk == 0 ? slot0 : 0)) * p.G;
+      };
+      // lane g < G: running max and sum of head g over the pieces
+      float Mu = -INFINITY, Lu = 0.0f;
+      if (lane < p.G) {
+#pragma unroll 4
+        for (int kk = 0; kk < np; ++kk) {
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + piece(kk) + lane);
+          if (ml.x > Mu) {
+            Lu *= fast_exp2(Mu - ml.x);
+            Mu = ml.x;
+          }
+          if (ml.x != -INFINITY) Lu += ml.y * fast_exp2(ml.x - Mu);
+        }
+      }
+      const float invL = Lu > 0.0f ? 1.0f / Lu : 0.0f;
+      // lane holds d = 4*lane..4*lane+3 of every head; a piece's weight
+      // comes from its head's lane
+      const float4* po = reinterpret_cast<const float4*>(p.part_o);
+      float4 acc[kMaxG];
+#pragma unroll
+      for (int jj = 0; jj < kMaxG; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int kk = 0; kk < np; ++kk) {      // a piece's vectors per round trip
+        float f = 0.0f;
+        if (lane < p.G && Mu != -INFINITY)
+          f = fast_exp2(__ldcg(&p.part_ml[(piece(kk) + lane) * 2]) - Mu);
+        float4 x[kMaxG];
+#pragma unroll
+        for (int jj = 0; jj < kMaxG; ++jj)
+          x[jj] = jj < p.G ? __ldcg(po + (piece(kk) + jj) * (kD / 4) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int jj = 0; jj < kMaxG; ++jj) {
+          const float wj = __shfl_sync(0xffffffffu, f, jj);
+          acc[jj].x += wj * x[jj].x; acc[jj].y += wj * x[jj].y;
+          acc[jj].z += wj * x[jj].z; acc[jj].w += wj * x[jj].w;
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < kMaxG; ++jj) {
+        const float r = __shfl_sync(0xffffffffu, invL, jj);
+        if (jj < p.G) {
+          uint2 pk;
+          pk.x = pack_bf16(acc[jj].x * r, acc[jj].y * r);
+          pk.y = pack_bf16(acc[jj].z * r, acc[jj].w * r);
+          *reinterpret_cast<uint2*>(outu + jj * kD + 4 * lane) = pk;
+        }
+      }
+      if (lane == 0) p.tickets[u] = 0;       // ready for the next call
+    }
+    return;
+  }
+
+  if (warp == kProducerWarp) {
+    // ---------------- producer warp ----------------------------------------
+    // The warp reads and compacts the rows; lane 0 alone issues the copies.
+    int st = 0;                 // stages issued (lane 0)
+    bool ok = true;
+    int cur_row = -1, cnt = 0, seq_len = 0;
+    int pgc[4], slc[4];        // the row's first 128 entries, kept for the second pass
+
+    auto acquire = [&](int s) -> bool {      // lane 0: stage slot s % NST is free
+      return s < NST || mbar_wait(&empty[s % NST], ((s / NST) - 1) & 1, &s_abort);
+    };
+    auto issue_marker = [&](int kind, int unit) -> bool {   // lane 0
+      if (!acquire(st)) return false;
+      const int sb = st % NST;
+      meta[sb] = make_int4(kind, 0, unit, 0);
+      mbar_arrive(&full[sb]);
+      ++st;
+      return true;
+    };
+
+    // lane 0: one page of K and V (one KV head), its fp8 scales and, on the
+    // first page of a piece, the unit's q rows
+    auto issue_page = [&](int2 ent, int flags, int unit, int h, int layer, int seq_len) -> bool {
+      if (!acquire(st)) return false;
+      const int sb = st % NST;
+      const int nvalid = max(0, min(P, seq_len - ent.x * P));
+      meta[sb] = make_int4(flags, nvalid, unit, 0);
       uint8_t* stage = ring + sb * C::kStageBytes;
-      mbar_arrive_expect_tx(&full[sb], 2 * C::kTileBytes + C::kScaleBytes);
+      const uint32_t qbytes = (flags & kFirst) ? (uint32_t)p.G * kD * 2 : 0u;
+      mbar_arrive_expect_tx(&full[sb], 2 * C::kTileBytes + C::kScaleBytes + qbytes);
+      const int row_k = ((layer * p.S + ent.y) * p.Hkv + h) * P;
       if (FP8) {
         tma_load_2d(stage, &tmK, &full[sb], 0, row_k);
-        const int row_v = ((layer * p.S + e.y) * p.Hkv + h) * kD;
+        const int row_v = ((layer * p.S + ent.y) * p.Hkv + h) * kD;
         tma_load_2d(stage + C::kTileBytes, &tmV, &full[sb], 0, row_v);
-        const size_t so = ((size_t)layer * p.S + e.y) * P;
+        const size_t so = ((size_t)layer * p.S + ent.y) * P;
         bulk_load(stage + 2 * C::kTileBytes, p.k_scale + so, P * 4, &full[sb]);
         bulk_load(stage + 2 * C::kTileBytes + P * 4, p.v_scale + so, P * 4, &full[sb]);
       } else {
@@ -194,29 +388,96 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         tma_load_2d(stage + C::kTileBytes, &tmV, &full[sb], 0, row_k);
         tma_load_2d(stage + C::kTileBytes + P * 128, &tmV, &full[sb], 64, row_k);
       }
-      ++issued;
+      if (qbytes) bulk_load(stage + C::kQOff, p.q + (size_t)unit * p.G * kD, qbytes, &full[sb]);
+      ++st;
+      return true;
+    };
+
+    for (int u = u_first; u <= u_last && ok; ++u) {
+      const int us = u * p.w;
+      const int a = max(t0, us) - us;
+      const int e = min(t1, us + p.w) - us;
+      const int row = u / p.Hkv, h = u - row * p.Hkv;
+      const int li = row / p.B, b = row - li * p.B;
+      const int layer = p.layer0 + li;
+      const int32_t* selr = p.sel + (size_t)row * p.W;
+      const int32_t* physr = p.phys + (size_t)row * p.W;
+      if (row != cur_row) {      // count the row's valid entries (once per row)
+        cur_row = row;
+        seq_len = p.seq_lens[b];
+        cnt = 0;
+        for (int base = 0; base < p.W; base += 4 * 32) {
+          int pg[4], sl[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {        // every load of the batch in flight at once
+            const int i = base + 32 * k + lane;
+            pg[k] = i < p.W ? selr[i] : -1;
+            sl[k] = i < p.W ? physr[i] : -1;
+            if (base == 0) { pgc[k] = pg[k]; slc[k] = sl[k]; }
+          }
+          int bad = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const bool valid = pg[k] >= 0 && sl[k] >= 0 && sl[k] < p.S;
+            if (pg[k] >= 0 && sl[k] < 0) bad |= SSA_ST_UNRESOLVED;
+            if (pg[k] >= 0 && sl[k] >= p.S) bad |= SSA_ST_BAD_ID;
+            cnt += __popc(__ballot_sync(0xffffffffu, valid));
+          }
+          if (bad) set_status(p.status, bad);
+        }
+      }
+      // this piece's share [a, e) of the unit's weight, as valid entries [j0, j1)
+      const int j0 = (int)((long long)a * cnt / p.w), j1 = (int)((long long)e * cnt / p.w);
+      if (j0 == j1) {
+        if (lane == 0) ok = issue_marker(kEmpty | (u == u_last ? kFinal : 0), u);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        continue;
+      }
+      int seen = 0, issued = 0;
+      for (int base = 0; base < p.W && seen < j1 && ok; base += 4 * 32) {
+        int pgv[4], slv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = base + 32 * k + lane;
+          pgv[k] = base == 0 ? pgc[k] : (i < p.W ? selr[i] : -1);
+          slv[k] = base == 0 ? slc[k] : (i < p.W ? physr[i] : -1);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (seen >= j1 || !ok) break;
+          const bool valid = pgv[k] >= 0 && slv[k] >= 0 && slv[k] < p.S;
+          const unsigned lt = (1u << lane) - 1u;
+          const unsigned m = __ballot_sync(0xffffffffu, valid);
+          const int rank = seen + __popc(m & lt);
+          const bool in = valid && rank >= j0 && rank < j1;
+          const unsigned mi = __ballot_sync(0xffffffffu, in);
+          if (in) plist[__popc(mi & lt)] = make_int2(pgv[k], slv[k]);
+          __syncwarp();
+          if (lane == 0) {
+            const int nw = __popc(mi);
+            for (int x = 0; x < nw && ok; ++x, ++issued) {
+              const int flags = (issued == 0 ? kFirst : 0) |
+                                (issued == j1 - j0 - 1 ? (u == u_last ? kLast | kFinal : kLast) : 0);
+              ok = issue_page(plist[x], flags, u, h, layer, seq_len);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          __syncwarp();                        // the window is rewritten next round
+          seen += __popc(m);
+        }
+      }
     }
-    if (aborted) {
+    if (lane != 0) return;
+    if (ok) ok = issue_marker(kDone, 0);
+    if (!ok) {
       s_abort = 1;
       set_status(p.status, SSA_ST_TIMEOUT);
       // let every copy still in flight land before the CTA can exit
-      for (int st = issued > NST ? issued - NST : 0; st < issued; ++st)
-        mbar_wait(&full[st % NST], (st / NST) & 1, nullptr);
+      for (int s = st > NST ? st - NST : 0; s < st; ++s)
+        mbar_wait(&full[s % NST], (s / NST) & 1, nullptr);
     }
     return;
   }
-
-  // the G query rows of this KV head (rows >= G are zero)
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.q + (((size_t)li * p.B + b) * p.Hq + (size_t)h * p.G) * kD);
-    uint4* dst = reinterpret_cast<uint4*>(qs);
-    for (int i = tid; i < kMaxG * kD / 8; i += kConsumerWarps * 32) {
-      const int g = i / (kD / 8);
-      dst[i] = g < p.G ? src[i] : make_uint4(0, 0, 0, 0);
-    }
-  }
-  consumer_sync();
 
   // ---------------- consumers -------------------------------------------------
   // QK^T: A = 16 K rows (tokens), B = q^T (8 heads), C = S^T[token][head].
@@ -224,49 +485,21 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   //       movmatrix), C = O^T[d][head].  No MMA row is padding.
   const int r4 = lane >> 2, c = lane & 3;
 
-  // q^T as the B operand: b0 = q[r4][k 2c, 2c+1], b1 = q[r4][k 2c+8, 2c+9];
-  // fp8: logical k pairs map to 4 consecutive bytes of K (d = 16ks+4c..+3)
   uint32_t qb[8][2];
   float qscale_log2 = p.sm_log2;
-  if (FP8) {
-    float amax = 0.0f;
-    for (int i = lane; i < kMaxG * kD; i += 32) amax = fmaxf(amax, fabsf(__bfloat162float(qs[i])));
-    amax = warp_max(amax);
-    int eq = 0;
-    if (amax > 0.0f) {
-      const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);     // amax in [2^(ef-127), 2^(ef-126))
-      eq = 141 - ef;                                                  // amax * 2^eq < 2^15
-      eq = eq > 126 ? 126 : (eq < -126 ? -126 : eq);
-    }
-    const float up = exp2f((float)eq);
-    qscale_log2 = p.sm_log2 * exp2f((float)-eq);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const __nv_bfloat16* r = qs + r4 * kD + 16 * ks + 4 * c;
-      qb[ks][0] = pack_f16(__bfloat162float(r[0]) * up, __bfloat162float(r[1]) * up);
-      qb[ks][1] = pack_f16(__bfloat162float(r[2]) * up, __bfloat162float(r[3]) * up);
-    }
-  } else {
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qb[ks][0] = *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c);
-      qb[ks][1] = *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c + 8);
-    }
-  }
-
-  list_wait();              // the producer's page list
-  const int nv = s_nv;
-  const int i0 = (int)((long long)nv * split / p.splits);
-  const int nst = (int)((long long)nv * (split + 1) / p.splits) - i0;
-
   float o[8][4];   // O^T: rows d = 16*mt + r4 (+8), columns (heads) 2c, 2c+1
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
   // softmax state of heads 2c, 2c+1 (the lanes that own those O^T columns);
   // fp8: probabilities carry v_scale / vref, vref a power of two above every
   // V scale seen so far (0 before the first block)
-  float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.0f, l_run1 = 0.0f;
-  float vref = FP8 ? 0.0f : 1.0f;
+  float m_run0, m_run1, l_run0, l_run1, vref;
+  auto reset = [&]() {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+    m_run0 = m_run1 = -INFINITY;
+    l_run0 = l_run1 = 0.0f;
+    vref = FP8 ? 0.0f : 1.0f;
+  };
+  reset();
   const int rot = c >= 2 ? 16 : 0;      // fp8 V: lanes 2, 3 hold the token pairs swapped
   // token of MMA row r4 and r4+8 within a 16-token block.  fp8: rows 2j, 2j+1
   // and 2j+8, 2j+9 cover the 4 consecutive tokens 4j..4j+3 that one 32-bit V
@@ -279,275 +512,463 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     tauB = 4 * j + (j < 2 ? 2 + e : e);
   }
 
-  for (int st = 0; st < nst; ++st) {
-    const int sb = st % NST;
-    if (!mbar_wait(&full[sb], (st / NST) & 1, &s_abort)) {
-      s_abort = 1;
-      set_status(p.status, SSA_ST_TIMEOUT);
-      break;
+  // End of a piece: leave this warp's state in comb for the merge warp
+  // (once it has read the previous piece's) and stream on.  The consumer
+  // warps never wait for one another.
+  int n_flush = 0;
+  auto flush = [&]() -> bool {
+    float l0 = l_run0, l1 = l_run1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    const int2 e = plist[i0 + st];
-    const int nvalid = max(0, min(P, seq_len - e.x * P));
-    uint8_t* stage = ring + sb * C::kStageBytes;
-    const uint32_t kb = smem_u32(stage);
-    const uint32_t vb = kb + C::kTileBytes;
-    const float* ksc = reinterpret_cast<const float*>(stage + 2 * C::kTileBytes);
-    const float* vsc = ksc + P;
+    if (n_flush > 0 && !mbar_wait(cfree, (n_flush - 1) & 1, &s_abort)) return false;
+    float* cO = comb;                                             // [4][8][D]
+    float* cM = cO + kConsumerWarps * kMaxG * kD;                  // [4][8]
+    float* cL = cM + kConsumerWarps * kMaxG;                       // [4][8]
+    // row (warp, head g) of cO holds column d at d ^ (8 * ((g >> 1) & 3)):
+    // the 32 lanes of a store (heads 2c, columns r4 + 16 mt) hit 32 banks
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d = (16 * mt + r4) ^ (8 * c);
+      cO[(warp * kMaxG + 2 * c) * kD + d] = o[mt][0] * vref;
+      cO[(warp * kMaxG + 2 * c + 1) * kD + d] = o[mt][1] * vref;
+      cO[(warp * kMaxG + 2 * c) * kD + (d ^ 8)] = o[mt][2] * vref;
+      cO[(warp * kMaxG + 2 * c + 1) * kD + (d ^ 8)] = o[mt][3] * vref;
+    }
+    if (r4 == 0) {
+      cM[warp * kMaxG + 2 * c] = m_run0;
+      cM[warp * kMaxG + 2 * c + 1] = m_run1;
+      cL[warp * kMaxG + 2 * c] = l0;
+      cL[warp * kMaxG + 2 * c + 1] = l1;
+    }
+    reset();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cfull);
+    ++n_flush;
+    return true;
+  };
 
-#pragma unroll 1
-    for (int blk = 0; blk < C::kBlocks; ++blk) {
-      if (((st * C::kBlocks + blk) & (kConsumerWarps - 1)) != warp) continue;
-      const int tb = blk * 16;
-      // zero V of the tokens past seq_len (their bytes are not ours to trust)
-      if (nvalid < tb + 16) {
+  // The CTA's last piece: the consumer warps combine, publish and, when
+  // they hold the unit's last piece, merge it themselves (the merge warp is
+  // done by then; they would otherwise sit idle).
+  uint32_t cph = 0;
+  auto csync = [&]() -> bool {             // one arrival per warp, bounded wait
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cbar);
+    const bool ok = mbar_wait(cbar, cph, &s_abort);
+    cph ^= 1u;
+    return ok;
+  };
+  auto final_flush = [&](int unit) -> bool {
+    float l0 = l_run0, l1 = l_run1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    if (n_flush > 0 && !mbar_wait(cfree, (n_flush - 1) & 1, &s_abort)) return false;
+    float* cO = comb;
+    float* cM = cO + kConsumerWarps * kMaxG * kD;
+    float* cL = cM + kConsumerWarps * kMaxG;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d = (16 * mt + r4) ^ (8 * c);
+      cO[(warp * kMaxG + 2 * c) * kD + d] = o[mt][0] * vref;
+      cO[(warp * kMaxG + 2 * c + 1) * kD + d] = o[mt][1] * vref;
+      cO[(warp * kMaxG + 2 * c) * kD + (d ^ 8)] = o[mt][2] * vref;
+      cO[(warp * kMaxG + 2 * c + 1) * kD + (d ^ 8)] = o[mt][3] * vref;
+    }
+    if (r4 == 0) {
+      cM[warp * kMaxG + 2 * c] = m_run0;
+      cM[warp * kMaxG + 2 * c + 1] = m_run1;
+      cL[warp * kMaxG + 2 * c] = l0;
+      cL[warp * kMaxG + 2 * c + 1] = l1;
+    }
+    if (!csync()) return false;
+    const int us = unit * p.w;
+    const int c_first = cta_of(p, us), c_last = cta_of(p, us + p.w - 1);
+    const bool whole = c_first == c_last;
+    const size_t pslot = (size_t)cta * 2 + (t0 >= us ? 0 : 1);
+    __nv_bfloat16* outu = p.out + (size_t)unit * p.G * kD;
+    // thread tid owns column d = tid of every head: 8 independent chains
+    const int d = tid;
+#pragma unroll
+    for (int gg = 0; gg < kMaxG; ++gg) {
+      if (gg < p.G) {
+        const int dz = d ^ (8 * ((gg >> 1) & 3));
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cM[w * kMaxG + gg]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float f = fast_exp2(cM[w * kMaxG + gg] - M);
+            L += cL[w * kMaxG + gg] * f;
+            O += cO[(w * kMaxG + gg) * kD + dz] * f;
+          }
+        }
+        if (whole) {
+          outu[gg * kD + d] = __float2bfloat16_rn(O * (L > 0.0f ? 1.0f / L : 0.0f));
+        } else {
+          const size_t pi = pslot * p.G + gg;
+          p.part_o[pi * kD + d] = O;
+          if (d == 0) {
+            p.part_ml[pi * 2] = M;
+            p.part_ml[pi * 2 + 1] = L;
+          }
+        }
+      }
+    }
+    if (whole) return true;
+    // publish: every partial write of the CTA, then one GPU-scope fence and
+    // the ticket
+    if (!csync()) return false;
+    if (tid == 0) {
+      __threadfence();
+      s_last = atomicAdd(&p.tickets[unit], 1) == c_last - c_first;
+    }
+    if (!csync()) return false;
+    if (!s_last) return true;
+    __threadfence();
+    const int np = c_last - c_first + 1;
+    const int slot0 = tile_begin(p, c_first) == us ? 0 : 1;
+    auto piece = [&](int kk) -> size_t {
+      return ((size_t)(c_first + kk) * 2 + (kk == 0 ? slot0 : 0)) * p.G;
+    };
+    // thread: d = 4*lane..+3 of heads warp and warp + 4; online merge of the
+    // pieces, two pieces' loads per round trip
+    const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
+    const float4* po = reinterpret_cast<const float4*>(p.part_o);
+    float Mh[2] = {-INFINITY, -INFINITY}, Lh[2] = {0.0f, 0.0f};
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int k0 = 0; k0 < np; k0 += 2) {
+      float2 ml[2][2];
+      float4 x[2][2];
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int g = warp + 4 * hh;
+          const bool ok = k0 + kk < np && g < p.G;
+          ml[kk][hh] = ok ? __ldcg(pml + piece(k0 + kk) + g) : make_float2(-INFINITY, 0.0f);
+          x[kk][hh] = ok ? __ldcg(po + (piece(k0 + kk) + g) * (kD / 4) + lane)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float m = ml[kk][hh].x;
+          if (m == -INFINITY) continue;
+          const float mn = fmaxf(Mh[hh], m);
+          const float a = fast_exp2(Mh[hh] - mn), b = fast_exp2(m - mn);
+          Lh[hh] = Lh[hh] * a + ml[kk][hh].y * b;
+          acc[hh].x = acc[hh].x * a + x[kk][hh].x * b;
+          acc[hh].y = acc[hh].y * a + x[kk][hh].y * b;
+          acc[hh].z = acc[hh].z * a + x[kk][hh].z * b;
+          acc[hh].w = acc[hh].w * a + x[kk][hh].w * b;
+          Mh[hh] = mn;
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int g = warp + 4 * hh;
+      if (g < p.G) {
+        const float r = Lh[hh] > 0.0f ? 1.0f / Lh[hh] : 0.0f;
+        uint2 pk;
+        pk.x = pack_bf16(acc[hh].x * r, acc[hh].y * r);
+        pk.y = pack_bf16(acc[hh].z * r, acc[hh].w * r);
+        *reinterpret_cast<uint2*>(outu + g * kD + 4 * lane) = pk;
+      }
+    }
+    if (tid == 0) p.tickets[unit] = 0;     // ready for the next call
+    return true;
+  };
+
+  // One call site for each flush, so that its code exists once.
+  int pc = 0;                              // pages processed
+  for (int st = 0;; ++st) {
+    int fkind = 0, funit = u_last;         // 1 = flush, 2 = final_flush
+    {
+      const int sb = st % NST;
+      if (!mbar_wait(&full[sb], (st / NST) & 1, &s_abort)) {
+        s_abort = 1;
+        set_status(p.status, SSA_ST_TIMEOUT);
+        break;
+      }
+      const int4 dsc = meta[sb];
+      if (dsc.x & kDone) break;
+      if (dsc.x & kEmpty) {
+        if (lane == 0) mbar_arrive(&empty[sb]);
+        fkind = (dsc.x & kFinal) ? 2 : 1;
+        funit = dsc.z;
+        goto flushes;
+      }
+      const int nvalid = dsc.y;
+      uint8_t* stage = ring + sb * C::kStageBytes;
+      const uint32_t kb = smem_u32(stage);
+      const uint32_t vb = kb + C::kTileBytes;
+      const float* ksc = reinterpret_cast<const float*>(stage + 2 * C::kTileBytes);
+      const float* vsc = ksc + P;
+
+      if (dsc.x & kFirst) {
+        // the unit's G query rows as the B operand (rows >= G are zero).
+        // bf16: b0 = q[r4][k 2c, 2c+1], b1 = q[r4][k 2c+8, 2c+9] per k16 step.
+        // fp8: q * 2^eq as two e4m3 terms hi + lo (the top and the next four
+        // significant bits: their sum is q * 2^eq to within 2^-10, i.e.
+        // ~2^-18 of |q|max), so QK runs as e4m3 MMAs on the raw K codes;
+        // per k32 step b0 = d 32ks + 4c..+3, b1 = d + 16; qb[ks] = hi,
+        // qb[4 + ks] = lo
+        const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(stage + C::kQOff);
+        const bool row_ok = r4 < p.G;
         if (FP8) {
-          for (int i = lane; i < kD * 16; i += 32) {
-            const int d = i >> 4, x = tb + (i & 15);
-            if (x >= nvalid) stage[C::kTileBytes + swz(d * P + x, C::kVSwz)] = 0;
+          float amax = 0.0f;
+          for (int i = lane; i < p.G * (kD / 8); i += 32)
+            amax = fmaxf(amax, bf16x8_absmax(*reinterpret_cast<const uint4*>(qs + i * 8)));
+          amax = warp_max(amax);
+          int eq = 0;
+          if (amax > 0.0f) {
+            const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);   // amax in [2^(ef-127), 2^(ef-126))
+            eq = 134 - ef;                                                // amax * 2^eq in [128, 256)
+            eq = eq > 126 ? 126 : (eq < -126 ? -126 : eq);
+          }
+          const float up = exp2f((float)eq);
+          qscale_log2 = p.sm_log2 * exp2f((float)-eq);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const __nv_bfloat16* r = qs + r4 * kD + 32 * ks + 16 * half + 4 * c;
+              float x[4], y[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) x[i] = row_ok ? __bfloat162float(r[i]) * up : 0.0f;
+              const uint32_t hi = f32x4_to_e4m3x4(x[0], x[1], x[2], x[3]);
+              e4m3x4_to_f32x4(hi, y[0], y[1], y[2], y[3]);
+              qb[ks][half] = hi;
+              qb[4 + ks][half] = f32x4_to_e4m3x4(x[0] - y[0], x[1] - y[1], x[2] - y[2], x[3] - y[3]);
+            }
           }
         } else {
-          for (int i = lane; i < 16 * 16; i += 32) {
-            const int r = tb + (i >> 4), ch = i & 15;
-            if (r >= nvalid)
-              *reinterpret_cast<uint4*>(stage + C::kTileBytes + (ch >> 3) * (P * 128) + r * 128 +
-                                        (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            qb[ks][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c) : 0u;
+            qb[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c + 8) : 0u;
           }
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
       }
 
-      // S^T = K q^T for 16 tokens; even and odd k-steps in two MMA chains
-      float s[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
-      const int tkA = tb + tauA, tkB = tb + tauB;
-      if (FP8) {
-        const uint32_t rA = kb + tkA * 128 + 4 * c, rB = kb + tkB * 128 + 4 * c;
-        const int xA = tkA & 7, xB = tkB & 7;
-#pragma unroll
-        for (int ks = 0; ks < 8; ks += 2) {
-          const uint32_t wA0 = lds32(rA + ((ks ^ xA) << 4));
-          const uint32_t wB0 = lds32(rB + ((ks ^ xB) << 4));
-          const uint32_t wA1 = lds32(rA + (((ks + 1) ^ xA) << 4));
-          const uint32_t wB1 = lds32(rB + (((ks + 1) ^ xB) << 4));
-          uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-          e4m3x4_to_f16x2x2(wA0, a0, a2);
-          e4m3x4_to_f16x2x2(wB0, a1, a3);
-          e4m3x4_to_f16x2x2(wA1, a4, a6);
-          e4m3x4_to_f16x2x2(wB1, a5, a7);
-          mma_f16(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-          mma_f16(sx, a4, a5, a6, a7, qb[ks + 1][0], qb[ks + 1][1]);
+      // NB 16-token blocks per warp step share one softmax update (max,
+      // rescale, V-scale reference) and interleave their MMA chains.  Two per
+      // step measured no faster than one on GB300 and needs more registers
+      // than two CTAs per SM leave, so one.
+      constexpr int NB = 1;
+      constexpr int kSteps = C::kBlocks / NB;
+#pragma unroll 1
+      for (int bs = 0; bs < kSteps; ++bs) {
+        if (((pc * kSteps + bs) & (kConsumerWarps - 1)) != warp) continue;
+        const int tb0 = bs * NB * 16;
+        // zero V of the tokens past seq_len (their bytes are not ours to trust)
+        if (nvalid < tb0 + NB * 16) {
+          for (int j = 0; j < NB; ++j) {
+            const int tb = tb0 + 16 * j;
+            if (nvalid >= tb + 16) continue;
+            if (FP8) {
+              for (int i = lane; i < kD * 16; i += 32) {
+                const int d = i >> 4, xx = tb + (i & 15);
+                if (xx >= nvalid) stage[C::kTileBytes + swz(d * P + xx, C::kVSwz)] = 0;
+              }
+            } else {
+              for (int i = lane; i < 16 * 16; i += 32) {
+                const int r = tb + (i >> 4), ch = i & 15;
+                if (r >= nvalid)
+                  *reinterpret_cast<uint4*>(stage + C::kTileBytes + (ch >> 3) * (P * 128) +
+                                            r * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+              }
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
         }
-      } else {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int t = tb + (mi & 1) * 8 + rr;
-        const uint32_t rowk = kb + t * 128;
-        const int xt = t & 7;
-#pragma unroll
-        for (int ks = 0; ks < 8; ks += 2) {
-          uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-          const int c0 = 2 * ks + (mi >> 1), c1 = c0 + 2;     // 16-byte chunks over d
-          ldsm_x4(a0, a1, a2, a3, rowk + (c0 >> 3) * (P * 128) + (((c0 & 7) ^ xt) << 4));
-          ldsm_x4(a4, a5, a6, a7, rowk + (c1 >> 3) * (P * 128) + (((c1 & 7) ^ xt) << 4));
-          mma_bf16(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-          mma_bf16(sx, a4, a5, a6, a7, qb[ks + 1][0], qb[ks + 1][1]);
-        }
-      }
-      // rows: s[0], s[1] = token tkA, heads 2c, 2c+1; s[2], s[3] = token tkB
-      float x0 = (s[0] + sx[0]) * qscale_log2, x1 = (s[1] + sx[1]) * qscale_log2;
-      float x2 = (s[2] + sx[2]) * qscale_log2, x3 = (s[3] + sx[3]) * qscale_log2;
-      float vsA = 0.0f, vsB = 0.0f;
-      if (FP8) {
-        const float kA = ksc[tkA], kB = ksc[tkB];
-        x0 *= kA; x1 *= kA; x2 *= kB; x3 *= kB;
-        vsA = vsc[tkA];
-        vsB = vsc[tkB];
-      }
-      if (nvalid < tb + 16) {          // the tail of a request's last page
-        if (tkA >= nvalid) { x0 = x1 = -INFINITY; vsA = 0.0f; }
-        if (tkB >= nvalid) { x2 = x3 = -INFINITY; vsB = 0.0f; }
-      }
-      // per-head maxima over the 16 tokens: the 8 lanes r4 = 0..7 of this c
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
-      const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
-      const float corr0 = fast_exp2(m_run0 - mu0), corr1 = fast_exp2(m_run1 - mu1);
-      float oc0 = corr0, oc1 = corr1;
-      float vinv = 1.0f;
-      if (FP8) {
-        float vmax = fmaxf(vsA, vsB);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1)
-          vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
-        if (vmax >= vref) {
-          const float nref = __uint_as_float(((__float_as_uint(vmax) >> 23) + 1) << 23);
-          const float ratio = vref * pow2_rcp(nref);
-          oc0 *= ratio;
-          oc1 *= ratio;
-          vref = nref;
-        }
-        vinv = pow2_rcp(vref);
-      }
-      const float p0 = fast_exp2(x0 - mu0), p1 = fast_exp2(x1 - mu1);
-      const float p2 = fast_exp2(x2 - mu0), p3 = fast_exp2(x3 - mu1);
-      uint32_t P0, P1;
-      if (FP8) {
-        l_run0 = l_run0 * corr0 + (p0 + p2);
-        l_run1 = l_run1 * corr1 + (p1 + p3);
-        const float wA = vsA * vinv, wB = vsB * vinv;
-        P0 = pack_f16(p0 * wA, p1 * wA);
-        P1 = pack_f16(p2 * wB, p3 * wB);
-      } else {
-        const float q0 = bf16_round(p0), q1 = bf16_round(p1);
-        const float q2 = bf16_round(p2), q3 = bf16_round(p3);
-        l_run0 = l_run0 * corr0 + (q0 + q2);
-        l_run1 = l_run1 * corr1 + (q1 + q3);
-        P0 = pack_bf16(q0, q1);
-        P1 = pack_bf16(q2, q3);
-      }
-      m_run0 = mn0;
-      m_run1 = mn1;
-      if (__any_sync(0xffffffffu, oc0 != 1.0f || oc1 != 1.0f)) {
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][0] *= oc0; o[mt][1] *= oc1; o[mt][2] *= oc0; o[mt][3] *= oc1;
-        }
-      }
-      // P^T as the B operand: each 8x8 half transposed across the warp
-      const uint32_t b0 = movmatrix_trans(P0), b1 = movmatrix_trans(P1);
 
-      // O^T += V^T P^T, 16 rows of d per MMA
-      if (FP8) {
-        // rows d = 16*mt + r4 and +8: the swizzle bits do not depend on mt
-        // (16*P*mt is a multiple of the swizzle period), so hoist them
-        const uint32_t va0 = vb + swz(r4 * P + tb + 4 * c, C::kVSwz);
-        const uint32_t va1 = vb + swz((r4 + 8) * P + tb + 4 * c, C::kVSwz);
+        // S^T = K q^T per block; rows: x[j][0], x[j][1] = token tkA[j], heads
+        // 2c, 2c+1; x[j][2], x[j][3] = token tkB[j]
+        float x[NB][4], vsA[NB], vsB[NB];
+        int tkA[NB], tkB[NB];
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          uint32_t w0 = lds32(va0 + mt * 16 * P);
-          uint32_t w1 = lds32(va1 + mt * 16 * P);
-          w0 = __funnelshift_l(w0, w0, rot);
-          w1 = __funnelshift_l(w1, w1, rot);
-          uint32_t a0, a1, a2, a3;
-          e4m3x4_to_f16x2x2(w0, a0, a2);
-          e4m3x4_to_f16x2x2(w1, a1, a3);
-          mma_f16(o[mt], a0, a1, a2, a3, b0, b1);
+        for (int j = 0; j < NB; ++j) {
+          const int tb = tb0 + 16 * j;
+          float s4[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
+          tkA[j] = tb + tauA;
+          tkB[j] = tb + tauB;
+          if (FP8) {
+            // A = the K codes as they are: a0/a2 = token tkA, d 32ks + 4c..+3
+            // and d + 16; a1/a3 = token tkB.  hi and lo terms in one chain
+            // (the step's blocks run as independent chains).
+            const uint32_t rA = kb + tkA[j] * 128 + 4 * c, rB = kb + tkB[j] * 128 + 4 * c;
+            const int xA = tkA[j] & 7, xB = tkB[j] & 7;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t a0 = lds32(rA + (((2 * ks) ^ xA) << 4));
+              const uint32_t a1 = lds32(rB + (((2 * ks) ^ xB) << 4));
+              const uint32_t a2 = lds32(rA + (((2 * ks + 1) ^ xA) << 4));
+              const uint32_t a3 = lds32(rB + (((2 * ks + 1) ^ xB) << 4));
+              mma_e4m3(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              mma_e4m3(s4, a0, a1, a2, a3, qb[4 + ks][0], qb[4 + ks][1]);
+            }
+          } else {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int t = tb + (mi & 1) * 8 + rr;
+            const uint32_t rowk = kb + t * 128;
+            const int xt = t & 7;
+#pragma unroll
+            for (int ks = 0; ks < 8; ks += 2) {
+              uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+              const int c0 = 2 * ks + (mi >> 1), c1 = c0 + 2;     // 16-byte chunks over d
+              ldsm_x4(a0, a1, a2, a3, rowk + (c0 >> 3) * (P * 128) + (((c0 & 7) ^ xt) << 4));
+              ldsm_x4(a4, a5, a6, a7, rowk + (c1 >> 3) * (P * 128) + (((c1 & 7) ^ xt) << 4));
+              mma_bf16(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              mma_bf16(sx, a4, a5, a6, a7, qb[ks + 1][0], qb[ks + 1][1]);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) x[j][i] = (s4[i] + sx[i]) * qscale_log2;
+          vsA[j] = vsB[j] = 0.0f;
+          if (FP8) {
+            const float kA = ksc[tkA[j]], kB = ksc[tkB[j]];
+            x[j][0] *= kA; x[j][1] *= kA; x[j][2] *= kB; x[j][3] *= kB;
+            vsA[j] = vsc[tkA[j]];
+            vsB[j] = vsc[tkB[j]];
+          }
+          if (nvalid < tb + 16) {          // the tail of a request's last page
+            if (tkA[j] >= nvalid) { x[j][0] = x[j][1] = -INFINITY; vsA[j] = 0.0f; }
+            if (tkB[j] >= nvalid) { x[j][2] = x[j][3] = -INFINITY; vsB[j] = 0.0f; }
+          }
         }
-      } else {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int t = tb + (mi >> 1) * 8 + rr;
+        // per-head maxima over the step's tokens: the 8 lanes r4 = 0..7 of c
+        float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int chunk = 2 * mt + (mi & 1);
-          const uint32_t addr =
-              vb + (chunk >> 3) * (P * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(a0, a1, a2, a3, addr);
-          mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
+        for (int j = 1; j < NB; ++j) {
+          mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][2]));
+          mx1 = fmaxf(mx1, fmaxf(x[j][1], x[j][3]));
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
+        const float corr0 = fast_exp2(m_run0 - mu0), corr1 = fast_exp2(m_run1 - mu1);
+        float oc0 = corr0, oc1 = corr1;
+        float vinv = 1.0f;
+        if (FP8) {
+          float vmax = fmaxf(vsA[0], vsB[0]);
+#pragma unroll
+          for (int j = 1; j < NB; ++j) vmax = fmaxf(vmax, fmaxf(vsA[j], vsB[j]));
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1)
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+          if (vmax >= vref) {
+            const float nref = __uint_as_float(((__float_as_uint(vmax) >> 23) + 1) << 23);
+            const float ratio = vref * pow2_rcp(nref);
+            oc0 *= ratio;
+            oc1 *= ratio;
+            vref = nref;
+          }
+          vinv = pow2_rcp(vref);
+        }
+        uint32_t b0[NB], b1[NB];
+        float ls0 = 0.0f, ls1 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          const float p0 = fast_exp2(x[j][0] - mu0), p1 = fast_exp2(x[j][1] - mu1);
+          const float p2 = fast_exp2(x[j][2] - mu0), p3 = fast_exp2(x[j][3] - mu1);
+          uint32_t P0, P1;
+          if (FP8) {
+            ls0 += p0 + p2;
+            ls1 += p1 + p3;
+            const float wA = vsA[j] * vinv, wB = vsB[j] * vinv;
+            P0 = pack_f16(p0 * wA, p1 * wA);
+            P1 = pack_f16(p2 * wB, p3 * wB);
+          } else {
+            const float q0 = bf16_round(p0), q1 = bf16_round(p1);
+            const float q2 = bf16_round(p2), q3 = bf16_round(p3);
+            ls0 += q0 + q2;
+            ls1 += q1 + q3;
+            P0 = pack_bf16(q0, q1);
+            P1 = pack_bf16(q2, q3);
+          }
+          // P^T as the B operand: each 8x8 half transposed across the warp
+          b0[j] = movmatrix_trans(P0);
+          b1[j] = movmatrix_trans(P1);
+        }
+        l_run0 = l_run0 * corr0 + ls0;
+        l_run1 = l_run1 * corr1 + ls1;
+        m_run0 = mn0;
+        m_run1 = mn1;
+        if (__any_sync(0xffffffffu, oc0 != 1.0f || oc1 != 1.0f)) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= oc0; o[mt][1] *= oc1; o[mt][2] *= oc0; o[mt][3] *= oc1;
+          }
+        }
+
+        // O^T += V^T P^T, 16 rows of d per MMA, the step's blocks in turn
+        if (FP8) {
+          // rows d = 16*mt + r4 and +8: the swizzle bits do not depend on mt
+          // (16*P*mt is a multiple of the swizzle period), so hoist them
+          uint32_t va0[NB], va1[NB];
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+            va0[j] = vb + swz(r4 * P + tb0 + 16 * j + 4 * c, C::kVSwz);
+            va1[j] = vb + swz((r4 + 8) * P + tb0 + 16 * j + 4 * c, C::kVSwz);
+          }
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              uint32_t w0 = lds32(va0[j] + mt * 16 * P);
+              uint32_t w1 = lds32(va1[j] + mt * 16 * P);
+              w0 = __funnelshift_l(w0, w0, rot);
+              w1 = __funnelshift_l(w1, w1, rot);
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x2x2(w0, a0, a2);
+              e4m3x4_to_f16x2x2(w1, a1, a3);
+              mma_f16(o[mt], a0, a1, a2, a3, b0[j], b1[j]);
+            }
+          }
+        } else {
+          const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              const int t = tb0 + 16 * j + (mi >> 1) * 8 + rr;
+              const int chunk = 2 * mt + (mi & 1);
+              const uint32_t addr =
+                  vb + (chunk >> 3) * (P * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_t(a0, a1, a2, a3, addr);
+              mma_bf16(o[mt], a0, a1, a2, a3, b0[j], b1[j]);
+            }
+          }
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[sb]);
-  }
-
-  // ---------------- merge the 4 warps' states (stage ring is idle now) ------
-  // l: sum over the 8 lanes (r4) that share heads 2c, 2c+1
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
-    l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
-  }
-  consumer_sync();
-  float* cO = reinterpret_cast<float*>(ring);                  // [4][8][D]
-  float* cM = cO + kConsumerWarps * kMaxG * kD;                 // [4][8]
-  float* cL = cM + kConsumerWarps * kMaxG;                      // [4][8]
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int d = 16 * mt + r4;
-    cO[(warp * kMaxG + 2 * c) * kD + d] = o[mt][0] * vref;
-    cO[(warp * kMaxG + 2 * c + 1) * kD + d] = o[mt][1] * vref;
-    cO[(warp * kMaxG + 2 * c) * kD + d + 8] = o[mt][2] * vref;
-    cO[(warp * kMaxG + 2 * c + 1) * kD + d + 8] = o[mt][3] * vref;
-  }
-  if (r4 == 0) {
-    cM[warp * kMaxG + 2 * c] = m_run0;
-    cM[warp * kMaxG + 2 * c + 1] = m_run1;
-    cL[warp * kMaxG + 2 * c] = l_run0;
-    cL[warp * kMaxG + 2 * c + 1] = l_run1;
-  }
-  consumer_sync();
-  const int unit = (li * p.B + b) * p.Hkv + h;
-  for (int i = tid; i < kMaxG * kD; i += kConsumerWarps * 32) {
-    const int gg = i / kD, d = i - gg * kD;
-    if (gg >= p.G) continue;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cM[w * kMaxG + gg]);
-    float L = 0.0f, O = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float f = fast_exp2(cM[w * kMaxG + gg] - M);
-        L += cL[w * kMaxG + gg] * f;
-        O += cO[(w * kMaxG + gg) * kD + d] * f;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[sb]);
+      ++pc;
+      if (dsc.x & kLast) {
+        fkind = (dsc.x & kFinal) ? 2 : 1;
+        funit = dsc.z;
       }
     }
-    if (p.splits == 1) {
-      const float r = L > 0.0f ? O / L : 0.0f;
-      p.out[(((size_t)li * p.B + b) * p.Hq + h * p.G + gg) * kD + d] = __float2bfloat16_rn(r);
-    } else {
-      const size_t pi = ((size_t)unit * p.splits + split) * p.G + gg;
-      p.part_o[pi * kD + d] = O;
-      if (d == 0) {
-        p.part_ml[pi * 2] = M;
-        p.part_ml[pi * 2 + 1] = L;
-      }
-    }
+  flushes:
+    if (fkind == 1 && !flush()) break;
+    if (fkind == 2 && !final_flush(funit)) break;
   }
-  if (p.splits == 1) return;
-
-  // ---------------- a7: the last CTA of this unit merges the splits ---------
-  // (an atomic ticket; no CTA ever waits for another)
-  __threadfence();
-  consumer_sync();
-  if (tid == 0) s_last = atomicAdd(&p.tickets[unit], 1) == p.splits - 1;
-  consumer_sync();
-  if (!s_last) return;
-  __threadfence();
-  // one pass: per head, the splits' weights exp2(m_s - M) and 1/L in shared
-  // memory (the ring is idle), then every output sums its splits' partials
-  float* sF = reinterpret_cast<float*>(ring);              // [splits][8]
-  float* sInvL = sF + p.splits * kMaxG;                     // [8]
-  const size_t ub = (size_t)unit * p.splits * p.G;
-  if (tid < p.G) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < p.splits; ++sp)
-      M = fmaxf(M, __ldcg(&p.part_ml[(ub + (size_t)sp * p.G + tid) * 2]));
-    float L = 0.0f;
-    for (int sp = 0; sp < p.splits; ++sp) {
-      const size_t pi = ub + (size_t)sp * p.G + tid;
-      const float f = M == -INFINITY ? 0.0f : fast_exp2(__ldcg(&p.part_ml[pi * 2]) - M);
-      sF[sp * kMaxG + tid] = f;
-      L += __ldcg(&p.part_ml[pi * 2 + 1]) * f;
-    }
-    sInvL[tid] = L > 0.0f ? 1.0f / L : 0.0f;
-  }
-  consumer_sync();
-  for (int i = tid; i < p.G * kD; i += kConsumerWarps * 32) {
-    const int gg = i / kD, d = i - gg * kD;
-    float O = 0.0f;
-#pragma unroll 4
-    for (int sp = 0; sp < p.splits; ++sp)
-      O += sF[sp * kMaxG + gg] * __ldcg(&p.part_o[(ub + (size_t)sp * p.G + gg) * kD + d]);
-    p.out[(((size_t)li * p.B + b) * p.Hq + h * p.G + gg) * kD + d] =
-        __float2bfloat16_rn(O * sInvL[gg]);
-  }
-  if (tid == 0) p.tickets[unit] = 0;     // ready for the next call
 }
 
 // ---------------------------------------------------------------------------
@@ -579,14 +1000,35 @@ bool make_tmap(CUtensorMap* tm, void* base, CUtensorMapDataType dt, int esz, uin
 }
 
 template <bool FP8, int P>
-size_t decode_smem(int W) {
+size_t decode_smem() {
   using C = Cfg<FP8, P>;
-  return 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)round_up(W, 2) * 8 +
-         kMaxG * kD * 2 + 2 * C::kStages * 8;
+  return 1024 + (size_t)C::kStages * C::kStageBytes + C::kCombineBytes + kWindow * 8 +
+         (size_t)C::kStages * 16 + 2 * C::kStages * 8 + 4 * 8;
+}
+
+// CTAs of one wave: resident CTAs per SM (the configuration's target, or
+// what the occupancy calculator grants, whichever is lower) x SMs, cut so
+// that every CTA gets at least two tiles and no unit more than 130 pieces.
+template <bool FP8, int P>
+int decode_grid(const Dims& d, int n_layers, int num_sms) {
+  static int occ = -1;
+  if (occ < 0) {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<FP8, P>, kDecodeThreads,
+                                                      decode_smem<FP8, P>()) != cudaSuccess)
+      o = 1;
+    occ = o < 1 ? 1 : (o > Cfg<FP8, P>::kCtasPerSm ? Cfg<FP8, P>::kCtasPerSm : o);
+  }
+  const int w = d.max_selected();
+  const long long T = (long long)n_layers * d.B * d.Hkv * w;
+  const int tpc_min = w > 256 ? (w + 127) / 128 : 2;
+  long long n = T / tpc_min;
+  if (n > (long long)num_sms * occ) n = (long long)num_sms * occ;
+  return n < 1 ? 1 : (int)n;
 }
 
 template <bool FP8, int P>
-cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeParams& p, cudaStream_t s) {
+cudaError_t launch_decode_t(const DecodeArgs& a, DecodeParams& p, cudaStream_t s) {
   const Dims& d = *a.d;
   const ssa_cache& c = *a.c;
   CUtensorMap tmK, tmV;
@@ -608,49 +1050,39 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const DecodeParams& p, cudaStre
                          CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return cudaErrorInvalidValue;
-  const size_t smem = decode_smem<FP8, P>(d.W);
+  const size_t smem = decode_smem<FP8, P>();
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP8, P>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.splits, d.B * d.Hkv, a.n_layers);
-  e = launch_pdl(decode_kernel<FP8, P>, grid, dim3(kDecodeThreads), smem, s, p, tmK, tmV);
+  const int n = decode_grid<FP8, P>(d, a.n_layers, a.num_sms);
+  if (n > decode_max_ctas(d, a.num_sms)) return cudaErrorInvalidValue;   // workspace bound
+  p.w = d.max_selected();
+  const long long T = (long long)a.n_layers * d.B * d.Hkv * p.w;
+  if (T > INT_MAX / 2) return cudaErrorInvalidValue;
+  p.T = (int)T;
+  p.tq = p.T / n;
+  p.tr = p.T % n;
+  e = launch_pdl(decode_kernel<FP8, P>, dim3(n), dim3(kDecodeThreads), smem, s, p, tmK, tmV);
   count_launch();
   return e;
 }
 
 }  // namespace
 
-// Resident CTAs per SM: the register cap of the launch bounds, or the
-// shared-memory footprint, whichever is tighter.
 int decode_ctas_per_sm(const Dims& d) {
-  size_t smem;
   switch (d.P * 2 + d.fp8) {
-    case 32: smem = decode_smem<false, 16>(d.W); break;
-    case 33: smem = decode_smem<true, 16>(d.W); break;
-    case 64: smem = decode_smem<false, 32>(d.W); break;
-    case 65: smem = decode_smem<true, 32>(d.W); break;
-    case 128: smem = decode_smem<false, 64>(d.W); break;
-    case 129: smem = decode_smem<true, 64>(d.W); break;
-    case 256: smem = decode_smem<false, 128>(d.W); break;
-    default: smem = decode_smem<true, 128>(d.W); break;
+    case 32: return Cfg<false, 16>::kCtasPerSm;
+    case 33: return Cfg<true, 16>::kCtasPerSm;
+    case 64: return Cfg<false, 32>::kCtasPerSm;
+    case 65: return Cfg<true, 32>::kCtasPerSm;
+    case 128: return Cfg<false, 64>::kCtasPerSm;
+    case 129: return Cfg<true, 64>::kCtasPerSm;
+    case 256: return Cfg<false, 128>::kCtasPerSm;
+    default: return Cfg<true, 128>::kCtasPerSm;
   }
-  const int by_regs = d.fp8 ? 3 : 2;
-  const int by_smem = (int)((228u * 1024u) / (smem + 1024u));
-  return by_smem < 1 ? 1 : (by_smem < by_regs ? by_smem : by_regs);
 }
 
-// Splits of each (layer, request, KV head) unit: as many as fill ONE wave of
-// resident CTAs (a partial second wave would double the tail), at least two
-// pages per split.
-int decode_splits(const Dims& d, int n_layers, int num_sms) {
-  const long long units = (long long)n_layers * d.B * d.Hkv;
-  const long long slots = (long long)num_sms * decode_ctas_per_sm(d);
-  long long s = slots / units;
-  const int max_s = d.max_selected() / 2 > 1 ? d.max_selected() / 2 : 1;
-  if (s > max_s) s = max_s;
-  if (s < 1) s = 1;
-  return (int)s;
-}
+int decode_max_ctas(const Dims& d, int num_sms) { return num_sms * decode_ctas_per_sm(d); }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   const Dims& d = *a.d;
@@ -669,7 +1101,6 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   p.status = a.status;
   p.layer0 = a.layer0;
   p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.G = d.G; p.W = d.W; p.S = d.S;
-  p.splits = a.splits;
   p.sm_log2 = a.sm_scale * 1.4426950408889634f;
   switch (d.P * 2 + d.fp8) {
     case 32: return launch_decode_t<false, 16>(a, p, s);

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
   __shared__ int tmp[33];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining, s_nv;
+  pdl_trigger();
   pdl_wait();
 
   const int li = blockIdx.x, layer = p.layer0 + li;
@@ -268,6 +269,7 @@ struct CopyParams {
 };
 
 __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(CopyParams p) {
+  pdl_trigger();
   pdl_wait();
   const int entry = blockIdx.y, li = blockIdx.z, layer = p.layer0 + li;
   if (entry >= p.n_miss[li] || p.k_mir == nullptr) return;
@@ -320,6 +322,7 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(CopyParams p) {
 __global__ void remap_kernel(const int32_t* slot_of, const int32_t* sel, const int32_t* bt,
                              int32_t* phys, int32_t* status, int layer0, int n_layers, int Lp,
                              int B, int W, int nmax) {
+  pdl_trigger();
   pdl_wait();
   const long long n = (long long)n_layers * B * W;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;

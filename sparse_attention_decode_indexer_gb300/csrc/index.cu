@@ -351,6 +351,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_topk_kernel(FusedParams p
   uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw + p.qg_bytes);   // [nmax]
   __shared__ float red[33];
   __shared__ int s_last;
+  pdl_trigger();
   pdl_wait();
   score_chunk<CPL>(p.s, qg, q8s, red);
   const int b = blockIdx.y, li = blockIdx.z;

@@ -20,9 +20,9 @@ struct Dims {
   int max_selected() const { return k + 1 < nmax ? k + 1 : nmax; }
 };
 
-// Split count of the attention kernel for a layer range (host heuristic);
-// the workspace holds partials for any count this returns.
-int decode_splits(const Dims& d, int n_layers, int num_sms);
+// Most CTAs one attention launch uses (one wave); the workspace holds two
+// partial states per CTA.
+int decode_max_ctas(const Dims& d, int num_sms);
 
 // -- store.cu ---------------------------------------------------------------
 cudaError_t launch_lru_init(const Dims& d, const ssa_cache& c, int identity, cudaStream_t s);
@@ -59,16 +59,16 @@ cudaError_t launch_remap(const Dims& d, const ssa_cache& c, int layer0, int n_la
 struct DecodeArgs {
   const Dims* d;
   const ssa_cache* c;
-  int layer0, n_layers, splits;
+  int layer0, n_layers, num_sms;
   const void* q;
   const int32_t* sel;
   const int32_t* phys;
   const int32_t* seq_lens;
   float sm_scale;
   void* out;
-  float* part_o;   // [units][splits][G][D]
-  float* part_ml;  // [units][splits][G][2]
-  int32_t* tickets;  // [units] split counters (zero before the first call; left zero)
+  float* part_o;   // [decode_max_ctas][2][G][D]
+  float* part_ml;  // [decode_max_ctas][2][G][2]
+  int32_t* tickets;  // [units] piece counters (zero before the first call; left zero)
   int32_t* status;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);

@@ -90,6 +90,28 @@ def reduce_max(x: float, dist, device) -> float:
     return float(t.item())
 
 
+# DRAM bytes (read + write) of one decode launch on lru_pressure_64k_fp8, from
+# the ncu capture summarised in profiles/decode_kernel_fp8_p64_lru_pressure_64k.md,
+# valid only for the kernel sources it was taken on (their SHA-256 below).
+DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53115904 + 327424,
+                  "sources": ("sparse_attention_decode_indexer_gb300/csrc/decode.cu",
+                              "sparse_attention_decode_indexer_gb300/csrc/common.cuh"),
+                  "sha256": "aefa31c23fd62a49359e24457c9f19a6a7d1e146f945dfc1edcd29582824bd54"}
+
+
+def decode_traffic(workload_name):
+    """The captured traffic per launch, or None when the workload differs or the
+    kernel sources changed since the capture."""
+    import hashlib
+    if workload_name != DECODE_TRAFFIC["workload"]:
+        return None
+    h = hashlib.sha256()
+    for f in DECODE_TRAFFIC["sources"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return DECODE_TRAFFIC["bytes"] if h.hexdigest() == DECODE_TRAFFIC["sha256"] else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -515,10 +537,10 @@ def run_ours(args, rank: int, world: int, dist):
                    "l2": "flushed between timed steps (256 MiB write + 256 MiB read)",
                    "host_warmup_steps": H,
                    "timing": timing_mode},
-        "roofline": {"kernel": "ssa_sparse_paged_decode (decode_kernel + merge_kernel)",
+        "roofline": {"kernel": "ssa_sparse_paged_decode (decode_kernel: attention and split merge)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"hbm_gbs of {peak_kind}",
-                     "traffic": None, "alg_bytes_per_launch": dec_bytes,
+                     "traffic": decode_traffic(w.name), "alg_bytes_per_launch": dec_bytes,
                      "avg_launch_us": 1e3 * dec_ms},
         "stages_us": {k: 1e3 * statistics.mean(v) for k, v in stage_ms.items()},
         "index_roofline": {"alg_bytes": index_bytes(w),

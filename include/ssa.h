@@ -255,10 +255,14 @@ int ssa_remap_block_table(const ssa_layout *lay, const ssa_cache *c, int layer0,
  * Entries with sel < 0 are padding; sel >= 0 with phys < 0 are skipped and
  * flagged SSA_ST_UNRESOLVED.  A request with no token gets zeros.
  *   q    [n_layers][B][Hq][D] bf16;  out [n_layers][B][Hq][D] bf16
- * Splits the pages of each (request, KV head) across CTAs (as many splits as
- * fill one wave of the GPU); the last CTA of each (layer, request, KV head)
- * to finish merges the partial softmax states, found by an atomic ticket.
- * ws holds the partials and the tickets (zeroed before first use).
+ * One wave of CTAs cuts the (layer, request, KV head) x page work into equal
+ * ranges (each (layer, request, KV head) weighs min(max_pages, block_topk+1)
+ * pages, the selection size of a request with at least block_topk + 1
+ * pages); a (layer, request, KV head) split between CTAs is merged by the
+ * last of its pieces to finish, found by an atomic ticket.  ws is required:
+ * it holds the partial softmax states and the tickets (zeroed before first
+ * use, left zero by every call that completes).  SSA_ERR_INVALID_ARG when
+ * ws is NULL.
  */
 int ssa_sparse_paged_decode(const ssa_layout *lay, const ssa_cache *c, int layer0, int n_layers,
                             const void *q, const int32_t *sel, const int32_t *phys,

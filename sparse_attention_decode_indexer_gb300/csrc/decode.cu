@@ -805,8 +805,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           tkB[j] = tb + tauB;
           if (FP8) {
             // A = the K codes as they are: a0/a2 = token tkA, d 32ks + 4c..+3
-            // and d + 16; a1/a3 = token tkB.  hi and lo terms in one chain
-            // (the step's blocks run as independent chains).
+            // and d + 16; a1/a3 = token tkB.  hi and lo terms in two chains.
             const uint32_t rA = kb + tkA[j] * 128 + 4 * c, rB = kb + tkB[j] * 128 + 4 * c;
             const int xA = tkA[j] & 7, xB = tkB[j] & 7;
 #pragma unroll
@@ -816,7 +815,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
               const uint32_t a2 = lds32(rA + (((2 * ks + 1) ^ xA) << 4));
               const uint32_t a3 = lds32(rB + (((2 * ks + 1) ^ xB) << 4));
               mma_e4m3(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-              mma_e4m3(s4, a0, a1, a2, a3, qb[4 + ks][0], qb[4 + ks][1]);
+              mma_e4m3(sx, a0, a1, a2, a3, qb[4 + ks][0], qb[4 + ks][1]);
             }
           } else {
             const int mi = lane >> 3, rr = lane & 7;

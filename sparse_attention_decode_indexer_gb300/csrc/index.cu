@@ -21,7 +21,7 @@ namespace ssa {
 namespace {
 
 constexpr int kScoreThreads = 256;
-constexpr int kScoreIters = 4;     // pages per lane group per CTA (loads in flight)
+constexpr int kScoreIters = 8;     // pages per lane group per round (loads in flight)
 
 struct ScoreParams {
   const int8_t* slab;              // [Lyr][Lp][HD]
@@ -65,7 +65,7 @@ __device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, i
     qraw[j] = i < nq16 ? reinterpret_cast<const uint4*>(qb)[i] : make_uint4(0, 0, 0, 0);
   }
   int4 v[kScoreIters][CPL];
-  bool live[kScoreIters];
+  bool live[kScoreIters];          // a slab row was loaded (the id is in range)
   int ids[kScoreIters];
   auto load_ids = [&](int base) {
 #pragma unroll
@@ -74,21 +74,18 @@ __device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, i
       ids[it] = pg < p1 ? p.bt[(size_t)b * p.nmax + pg] : -1;
     }
   };
+  // the slab loads wait only for the ids (not for seq_len): a page past the
+  // request's length is masked, and a bad id flagged, when it is scored
   auto load_round = [&](int base) {
 #pragma unroll
     for (int it = 0; it < kScoreIters; ++it) {
       const int pg = base + it * groups + grp;
-      live[it] = false;
-      if (pg < p1 && pg < n_b) {
-        const int id = ids[it];
-        if (id >= 0 && id < p.Lp) {
-          live[it] = true;
-          const int4* row = reinterpret_cast<const int4*>(slab_l + (size_t)id * HD);
+      const int id = ids[it];
+      live[it] = pg < p1 && id >= 0 && id < p.Lp;
+      if (live[it]) {
+        const int4* row = reinterpret_cast<const int4*>(slab_l + (size_t)id * HD);
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) v[it][c] = __ldg(row + sub + c * L);
-        } else if (sub == 0) {
-          set_status(p.status, SSA_ST_BAD_ID);
-        }
+        for (int c = 0; c < CPL; ++c) v[it][c] = __ldg(row + sub + c * L);
       }
     }
   };
@@ -142,8 +139,11 @@ __device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, i
 #pragma unroll
     for (int it = 0; it < kScoreIters; ++it) {
       const int pg = base + it * groups + grp;
+      const bool in = pg < p1 && pg < n_b;
+      if (in && !live[it] && sub == 0) set_status(p.status, SSA_ST_BAD_ID);
+      const bool use = in && live[it];
       int acc = 0;
-      if (live[it]) {
+      if (use) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           const int w[4] = {v[it][c].x, v[it][c].y, v[it][c].z, v[it][c].w};
@@ -155,7 +155,7 @@ __device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, i
         }
       }
       for (int o = L >> 1; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (sub == 0 && pg < p1) out[pg] = live[it] ? acc : INT_MIN;
+      if (sub == 0 && pg < p1) out[pg] = use ? acc : INT_MIN;
     }
     base += groups * kScoreIters;
     if (base >= p1) break;
@@ -169,7 +169,7 @@ __host__ __device__ inline int qg_bytes(int HD) { return (HD * 2 + 15) / 16 * 16
 __host__ __device__ inline int q8_bytes(int HqD) { return (HqD + 15) / 16 * 16; }
 
 template <int CPL>
-__global__ void __launch_bounds__(kScoreThreads) index_score_kernel(ScoreParams p) {
+__global__ void __launch_bounds__(kScoreThreads, CPL == 1 ? 3 : 2) index_score_kernel(ScoreParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   int16_t* qg = reinterpret_cast<int16_t*>(smem_raw);
   int8_t* q8s = reinterpret_cast<int8_t*>(smem_raw + qg_bytes(p.Hkv * p.D));
@@ -344,7 +344,7 @@ struct FusedParams {
 };
 
 template <int CPL>
-__global__ void __launch_bounds__(kScoreThreads) index_topk_kernel(FusedParams p) {
+__global__ void __launch_bounds__(kScoreThreads, CPL == 1 ? 3 : 2) index_topk_kernel(FusedParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   int16_t* qg = reinterpret_cast<int16_t*>(smem_raw);
   int8_t* q8s = reinterpret_cast<int8_t*>(smem_raw + qg_bytes(p.s.Hkv * p.s.D));

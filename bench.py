@@ -93,10 +93,10 @@ def reduce_max(x: float, dist, device) -> float:
 # DRAM bytes (read + write) of one decode launch on lru_pressure_64k_fp8, from
 # the ncu capture summarised in profiles/decode_kernel_fp8_p64_lru_pressure_64k.md,
 # valid only for the kernel sources it was taken on (their SHA-256 below).
-DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53115904 + 327424,
+DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53115136 + 289792,
                   "sources": ("sparse_attention_decode_indexer_gb300/csrc/decode.cu",
                               "sparse_attention_decode_indexer_gb300/csrc/common.cuh"),
-                  "sha256": "aefa31c23fd62a49359e24457c9f19a6a7d1e146f945dfc1edcd29582824bd54"}
+                  "sha256": "c4aa80305fd9f4659e4cb8820dd3e4174c3cd24b33787657209f8e431a65eeff"}
 
 
 def decode_traffic(workload_name):

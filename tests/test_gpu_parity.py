@@ -52,6 +52,14 @@ SMALL = [
        fp8=True, block_topk=20, seed=109),
     # every page selected (dense attention), tiny requests
     _w("dense_short", batch=3, ctx=64 * 5, seq_lens=(64 * 5, 1, 64 + 1), block_topk=32, seed=110),
+    # many (layer, request, KV head) units per attention CTA: 512 units of 9
+    # pages over one wave, so CTAs hold whole units and pieces of two others
+    # (the mid-range merges); then ragged lengths, 1 token to full
+    _w("many_units_fp8", batch=64, ctx=64 * 40, n_q_heads=32, n_kv_heads=4, fp8=True,
+       block_topk=8, steps=2, rho=0.9, walk_c=math.sqrt(1 - 0.81), seed=111),
+    _w("many_units_bf16_ragged", batch=48, ctx=64 * 40,
+       seq_lens=tuple(64 * 40 if i % 3 == 0 else (i * 379) % (64 * 40) + 1 for i in range(48)),
+       block_topk=8, steps=2, rho=0.9, walk_c=math.sqrt(1 - 0.81), seed=112),
 ]
 
 

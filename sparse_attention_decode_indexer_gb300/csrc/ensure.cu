@@ -10,7 +10,9 @@
 //
 // Order of events per layer (the pages state none; this is the reading the
 // library takes, identical in the oracle):
-//   1. U = distinct selected logical ids, ascending (bitonic sort + dedup);
+//   1. U = distinct selected logical ids, ascending (a bitmap over the
+//      logical ids and a popcount scan; a bitonic sort + dedup when the
+//      bitmap does not fit the shared memory at hand);
 //   2. hits: last_use = clock;
 //   3. misses, ascending, take victims in order: free slots by slot id, then
 //      bound slots not touched this step by (last_use, slot) -- the m
@@ -96,22 +98,52 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
   int32_t* mslot = p.miss_slot + (size_t)li * BW;
   const int32_t clock = p.clock[layer];
 
-  // 1. gather selected logical ids, sort, dedup
-  for (int i = tid; i < N2; i += nt) {
-    uint32_t key = 0xFFFFFFFFu;
-    if (i < BW) {
-      const int b = i / p.W;
-      const int pg = p.sel[((size_t)li * p.B + b) * p.W + (i - b * p.W)];
-      if (pg >= 0) {
-        const int id = pg < p.nmax ? p.bt[(size_t)b * p.nmax + pg] : -1;
-        if (id >= 0 && id < p.Lp) key = (uint32_t)id;
-        else set_status(p.status, SSA_ST_BAD_ID);
+  // 1. the distinct selected logical ids, ascending, in ids[] (0xFFFFFFFF
+  //    after them)
+  auto selected_id = [&](int i) -> uint32_t {        // entry i of the batch's selection
+    const int b = i / p.W;
+    const int pg = p.sel[((size_t)li * p.B + b) * p.W + (i - b * p.W)];
+    if (pg < 0) return 0xFFFFFFFFu;
+    const int id = pg < p.nmax ? p.bt[(size_t)b * p.nmax + pg] : -1;
+    if (id >= 0 && id < p.Lp) return (uint32_t)id;
+    set_status(p.status, SSA_ST_BAD_ID);
+    return 0xFFFFFFFFu;
+  };
+  const int nw = (p.Lp + 31) / 32;
+  if (nw <= 2 * N2) {
+    // a bitmap over the logical ids (in the victim buffer, free until step
+    // 3): set a bit per selected id, then each thread emits the set bits of
+    // its words at its place in the popcount scan -- five barriers where a
+    // sort of N2 keys takes log2(N2)^2/2
+    uint32_t* bits = reinterpret_cast<uint32_t*>(vic);
+    for (int w = tid; w < nw; w += nt) bits[w] = 0u;
+    for (int i = tid; i < N2; i += nt) ids[i] = 0xFFFFFFFFu;
+    __syncthreads();
+    for (int i = tid; i < BW; i += nt) {
+      const uint32_t id = selected_id(i);
+      if (id != 0xFFFFFFFFu) atomicOr(&bits[id >> 5], 1u << (id & 31));
+    }
+    __syncthreads();
+    const int wper = (nw + nt - 1) / nt;
+    const int w0 = min(nw, tid * wper), w1 = min(nw, w0 + wper);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+    int nd;
+    int at = block_exclusive_scan(cnt, tmp, nd);
+    for (int w = w0; w < w1; ++w) {
+      uint32_t x = bits[w];
+      while (x) {
+        const int bit = __ffs(x) - 1;
+        ids[at++] = (uint32_t)(w * 32 + bit);
+        x &= x - 1u;
       }
     }
-    ids[i] = key;
+    __syncthreads();
+  } else {
+    for (int i = tid; i < N2; i += nt) ids[i] = i < BW ? selected_id(i) : 0xFFFFFFFFu;
+    __syncthreads();
+    bitonic_sort_smem(ids, N2);
   }
-  __syncthreads();
-  bitonic_sort_smem(ids, N2);
 
   // 2. hits are touched; misses ranked in ascending id order
   const int per = (N2 + nt - 1) / nt;

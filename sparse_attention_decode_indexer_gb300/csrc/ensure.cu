@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
   uint32_t* keys = ids + N2;                                                 // [S] (KEYS_IN_SMEM)
   __shared__ int hist[256];
   __shared__ int tmp[33];
-  __shared__ uint32_t s_prefix;
+  __shared__ uint32_t s_prefix, s_lo, s_hi;
   __shared__ int s_remaining, s_nv;
   pdl_trigger();
   pdl_wait();
@@ -171,21 +171,42 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
     if (KEYS_IN_SMEM) {
       for (int s = tid; s < p.S; s += nt) keys[s] = victim_key(page_of, last_use, s, clock);
     }
-    if (tid == 0) { s_prefix = 0; s_remaining = m; s_nv = 0; }
     auto key_of = [&](int s) -> uint32_t {
       return KEYS_IN_SMEM ? keys[s] : victim_key(page_of, last_use, s, clock);
     };
-    uint32_t mask = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    // the candidates' key range (slots touched this step, key 0xFFFFFFFF,
+    // are never victims): last_use values span a few hundred clocks, so
+    // bins over the range need one or two passes where the full 32 bits
+    // need four
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int s = tid; s < p.S; s += nt) {
+      const uint32_t kk = key_of(s);
+      if (kk != 0xFFFFFFFFu) { lo = min(lo, kk); hi = max(hi, kk); }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (tid == 0) { s_lo = 0xFFFFFFFFu; s_hi = 0u; s_remaining = m; s_nv = 0; }
+    __syncthreads();
+    if ((tid & 31) == 0) { atomicMin(&s_lo, lo); atomicMax(&s_hi, hi); }
+    __syncthreads();
+    // LSB-side radix search for the m-th smallest key within [base, span_hi]:
+    // bins of 8 bits of (key - base), from the highest bit the range uses
+    uint32_t base = s_lo, span_hi = s_hi;
+    const uint32_t range = s_hi - s_lo;
+    int shift = range == 0 ? 0 : max(0, 32 - __clz((int)range) - 8);
+    if (range >> 31) shift = 24;
+    for (;;) {
       for (int i = tid; i < 256; i += nt) hist[i] = 0;
       __syncthreads();
-      const uint32_t prefix = s_prefix;
-      for (int base = 0; base < p.S; base += nt) {        // uniform trip count
-        const int s = base + tid;
-        const uint32_t kk = s < p.S ? key_of(s) : 0u;
-        const bool use = s < p.S && (kk & mask) == prefix;
+      for (int b0 = 0; b0 < p.S; b0 += nt) {        // uniform trip count
+        const int s = b0 + tid;
+        const uint32_t kk = s < p.S ? key_of(s) : 0xFFFFFFFFu;
+        const bool use = s < p.S && kk >= base && kk <= span_hi && kk != 0xFFFFFFFFu;
         // one atomic per distinct bin per warp: last_use values cluster
-        const int key = use ? (int)((kk >> shift) & 255) : -1 - (tid & 31);
+        const int key = use ? (int)(((kk - base) >> shift) & 255) : -1 - (tid & 31);
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         if (use && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[key], __popc(peers));
       }
@@ -208,15 +229,18 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
           for (int j = 0; j < 8; ++j) {
             if (below + cnt[j] >= rem) {
               s_remaining = rem - below;
-              s_prefix = prefix | ((uint32_t)(8 * tid + j) << shift);
+              s_prefix = base + ((uint32_t)(8 * tid + j) << shift);
               break;
             }
             below += cnt[j];
           }
         }
       }
-      mask |= 0xFFu << shift;
       __syncthreads();
+      base = s_prefix;
+      if (shift == 0) break;
+      span_hi = (uint32_t)min((unsigned long long)base + ((1ull << shift) - 1ull), 0xFFFFFFFEull);
+      shift = shift >= 8 ? shift - 8 : 0;
     }
     const uint32_t T = s_prefix;
     const int need_eq = s_remaining;

@@ -579,6 +579,8 @@ def main():
         cb = cpu_oracle_sample(w, args.cpu_seconds * max(1, min(args.steps, 5)) / 5)
         line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT,
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                # one step = every layer of every request, at the sample's rate
+                "ms_per_step": 1e3 * w.n_layers * w.batch / cb["value"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64 attention, int32 indexer", "data": "synthetic",
                 "config": {"workload": w.name}, "cpu_baseline": cb,

@@ -22,26 +22,20 @@
 //     P tokens of K and V) into shared memory with TMA tiled copies (128-byte
 //     swizzle), plus the fp8 per-token scales with bulk copies, through an
 //     mbarrier ring.  Each stage carries a small descriptor (first/last page
-//     of a piece, valid tokens, unit, q slot).  Per unit the producer also
-//     writes the unit's G query rows, loaded one unit ahead, as the QK B
-//     operand into one of two q slots.  Empty pieces and the end of the range
-//     travel as stages without data;
-//   * QK^T on the 5th-generation tensor cores: one thread issues, per page,
-//     tcgen05 MMAs with M = 64 (A = the page's K rows straight from the TMA
-//     tile, tokens as rows), N = 16 (B = the q slot), accumulating S^T in
-//     TMEM (16 columns per stage), and commits them to the stage's barrier;
-//   * four consumer warps each take 16-token blocks: a warp reads its
-//     block's 16 TMEM lanes as the m16n8 fragment, runs the online softmax in
-//     the log2 domain with warp shuffles, and PV with d as the rows (A = V^T,
-//     B = P^T, the probabilities transposed in registers by movmatrix) in
-//     warp-level m16n8k16 MMAs, fp32 accumulate;
-//   * bf16 K/V: bf16 MMAs (kind::f16 for QK), V by ldmatrix.trans;
-//   * fp8 K/V: QK runs as kind::f8f6f4 e4m3 MMAs on the raw K codes, q scaled
-//     by a power of two and split into two e4m3 terms (hi, lo: the B rows 0-7
-//     and 8-15); the K scale multiplies the fp32 score.  The e4m3 V codes
-//     convert exactly to f16 for PV, and the V scale folds into the
-//     probabilities (relative to a running power-of-two reference, so the f16
-//     operand never overflows).  V is stored d-major in the pool
+//     of a piece, valid tokens, unit); the first page of a piece also brings
+//     the unit's G query rows.  Empty pieces and the end of the range travel
+//     as stages without data;
+//   * four consumer warps each take 16-token blocks: QK^T with the tokens as
+//     the MMA rows (A = K, B = q^T, N = 8 query heads) and PV with d as the
+//     rows (A = V^T, B = P^T, the probabilities transposed in registers by
+//     movmatrix), m16n8k16 tensor-core tiles, fp32 accumulate, online softmax
+//     in the log2 domain with warp shuffles;
+//   * bf16 K/V: bf16 MMAs, ldmatrix (V transposed by ldmatrix.trans);
+//   * fp8 K/V: the e4m3 codes convert exactly to f16, so the MMAs run in f16
+//     on the raw codes; q is scaled by a power of two into f16 range, the K
+//     scale multiplies the fp32 score, and the V scale folds into the
+//     probabilities (relative to a running power-of-two reference, so the
+//     f16 operand never overflows).  V is stored d-major in the pool
 //     ([Hkv][D][P]) so that the 8-bit reads run along tokens, the reduction
 //     axis of PV;
 //   * at the end of a piece each consumer warp leaves its softmax state in
@@ -54,7 +48,6 @@
 // the G-row tiles, the memory system sets the pace.
 #include <cudaTypedefs.h>
 #include <cuda.h>
-#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -70,8 +63,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kMergeWarp = kConsumerWarps + 1;
-constexpr int kMmaWarp = kConsumerWarps + 2;
-constexpr int kDecodeThreads = kConsumers + 96;
+constexpr int kDecodeThreads = kConsumers + 64;
 constexpr int kMaxG = 8;
 constexpr int kWindow = 32;          // producer compaction window (entries)
 constexpr int kMaxStages = 12;
@@ -92,28 +84,12 @@ template <bool FP8, int P>
 struct Cfg {
   static constexpr int kTileBytes = P * kD * (FP8 ? 1 : 2);      // one KV head of one page
   static constexpr int kScaleBytes = FP8 ? 2 * P * 4 : 0;
-  static constexpr int kStageBytes = round_up(2 * kTileBytes + kScaleBytes, 1024);
-  static constexpr int kCombineBytes =
-      round_up(kConsumerWarps * kMaxG * kD * 4 + 2 * kConsumerWarps * kMaxG * 4, 1024);
-  // the QK B operand of a unit: 16 rows (N) of q, K-major, 128-byte swizzle;
-  // fp8 one 128-byte slab (rows 0-7 the hi codes, 8-15 the lo codes), bf16
-  // two 64-column slabs (rows 8-15 zero).  Two slots: consecutive units.
-  static constexpr int kQTileBytes = FP8 ? 16 * 128 : 2 * 16 * 128;
-  // QK runs as M = 64 MMAs (P = 128: two, over the page's halves); below 64
-  // tokens the A operand starts up to 48 rows before the page so that its
-  // tokens land on the TMEM lanes of the warps that take them, and reads up
-  // to 64 rows from there: the shared memory before the ring (combine area,
-  // q slots) and kAOver bytes past the last stage must exist
-  static constexpr int kHalves = P == 128 ? 2 : 1;
-  static constexpr int kRowsBefore = P < 64 ? 64 - P : 0;
-  static constexpr int kAOverRaw = (FP8 ? 64 * 128 : P * 128 + 64 * 128) - kStageBytes;
-  static constexpr int kAOver = P < 64 && kAOverRaw > 0 ? kAOverRaw : 0;
-  static constexpr int kNCols = 16;                               // D columns of one M = 64 MMA
-  static constexpr int kDCols = kNCols * kHalves;                 // per stage
-  // alignment slack, combine area, q slots, producer window, descriptors,
-  // barriers, over-read pad
-  static constexpr int kFixed = 1024 + kCombineBytes + 2 * kQTileBytes + kWindow * 8 +
-                                kMaxStages * 40 + 64 + kAOver;
+  static constexpr int kQOff = 2 * kTileBytes + kScaleBytes;
+  static constexpr int kQBytes = kMaxG * kD * 2;
+  static constexpr int kStageBytes = round_up(kQOff + kQBytes, 1024);
+  static constexpr int kCombineBytes = kConsumerWarps * kMaxG * kD * 4 + 2 * kConsumerWarps * kMaxG * 4;
+  // alignment slack, combine area, producer window, descriptors and barriers
+  static constexpr int kFixed = 1024 + kCombineBytes + kWindow * 8 + kMaxStages * 32 + 64;
   // two CTAs per SM when at least two stages fit beside the second CTA
   static constexpr int kStages2 = (kSmemPerSm / 2 - kSmemReservedPerCta - kFixed) / kStageBytes;
   static constexpr int kCtasPerSm = kStages2 >= 2 ? 2 : 1;
@@ -123,27 +99,8 @@ struct Cfg {
   static constexpr int kBlocks = P / 16;                          // 16-token blocks per page
   // log2 of the fp8 V^T row swizzle span in 16-byte units (row = P bytes)
   static constexpr int kVSwz = P >= 128 ? 3 : (P == 64 ? 2 : (P == 32 ? 1 : 0));
-  // TMEM columns: a power of two >= 32.  At most two CTAs of this kernel fit
-  // on an SM (shared memory), so two allocations of <= 256 columns never
-  // exceed the SM's 512 and an allocation never waits.
-  static constexpr int kTmemCols = kStages * kDCols <= 32    ? 32
-                                   : kStages * kDCols <= 64  ? 64
-                                   : kStages * kDCols <= 128 ? 128
-                                                             : 256;
-  // layout from the 1024-aligned base: combine area, q slots, the stage ring,
-  // producer window, stage descriptors, barriers (full, empty, sfull [NST];
-  // cfull, cfree, cbar), then the over-read pad
-  static constexpr int kOffQ = kCombineBytes;
-  static constexpr int kOffRing = kOffQ + 2 * kQTileBytes;
-  static constexpr int kOffPlist = kOffRing + kStages * kStageBytes;
-  static constexpr int kOffMeta = kOffPlist + kWindow * 8;
-  static constexpr int kOffBars = kOffMeta + kStages * 16;
-  static constexpr int kSmemBytes = 1024 + kOffBars + (3 * kStages + 3) * 8 + kAOver;
   static_assert(kStages >= 2, "at least two stages");
-  static_assert(kStages * kDCols <= 256, "TMEM: at most 256 columns per CTA");
-  static_assert(3 * kSmemBytes > kSmemPerSm, "a third CTA on the SM would overrun TMEM");
-  static_assert(kSmemBytes <= kSmemPerCtaMax, "shared memory");
-  static_assert(kRowsBefore * 128 <= kCombineBytes + 2 * kQTileBytes, "A over-read before the ring");
+  static_assert(kQOff % 16 == 0, "q rows need a 16-byte aligned bulk copy");
 };
 
 struct DecodeParams {
@@ -160,7 +117,6 @@ struct DecodeParams {
   int32_t* status;
   int T, tq, tr;             // tiles (units * w); CTA c holds [c*tq + min(c, tr), ...)
   int layer0, B, Hq, Hkv, G, W, S, w;
-  int k5d;                  // fp8 K map: 1 = one 5-D box per page, 0 = 3-D boxes of 8 rows
   float sm_log2;            // sm_scale * log2(e)
 };
 
@@ -174,111 +130,6 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
-}
-
-// 3-D and 5-D tiled TMA loads (the fp8 K pages: rows permuted within 16-token blocks)
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar,
-                                            int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(smem_u32(smem_dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_5d(void* smem_dst, const void* tmap, uint64_t* bar,
-                                            int c0, int c1, int c2, int c3, int c4) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-      ::"r"(smem_u32(smem_dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-        "r"(smem_u32(bar))
-      : "memory");
-}
-
-// ---- 5th-generation tensor cores (tcgen05): TMEM, MMA, TMEM -> registers ----
-// Allocation by one whole warp; the column base is written to shared memory.
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-               ::"r"(smem_u32(dst)), "r"(ncols) : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
-               ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major operand in the 128-byte
-// swizzle layout (rows of 128 bytes, 16-byte chunk j of row r at chunk
-// j ^ (r & 7), groups of 8 rows 1024 bytes apart).  A K step inside the
-// 128-byte row advances the start address; the swizzle is a function of the
-// address bits, so the tile base must be 1024-byte aligned.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4)     // start address >> 4
-         | (1ull << 16)                          // leading-dimension offset (unused when swizzled)
-         | ((uint64_t)(1024 >> 4) << 32)         // stride between 8-row groups
-         | (1ull << 46)                          // descriptor version
-         | (2ull << 61);                         // 128-byte swizzle
-}
-
-// Instruction descriptor: D f32, A and B K-major, M = 64, N = 16;
-// kind::f8f6f4 with e4m3 A and B, or kind::f16 with bf16 A and B.
-template <bool FP8>
-__device__ __forceinline__ constexpr uint32_t qk_idesc() {
-  return (1u << 4)                               // D format f32
-         | ((FP8 ? 0u : 1u) << 7)                // A: e4m3 / bf16
-         | ((FP8 ? 0u : 1u) << 10)               // B: e4m3 / bf16
-         | ((16u >> 3) << 17)                    // N >> 3
-         | ((64u >> 4) << 24);                   // M >> 4
-}
-
-// D[tmem] (+)= A B^T, one thread issues
-template <bool FP8>
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
-  if (FP8)
-    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n"
-                 ::"r"(d), "l"(a), "l"(b), "r"(qk_idesc<FP8>()), "r"(acc) : "memory");
-  else
-    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-                 ::"r"(d), "l"(a), "l"(b), "r"(qk_idesc<FP8>()), "r"(acc) : "memory");
-}
-
-// The mbarrier gets one arrival once every MMA this thread issued so far is done.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               ::"r"(smem_u32(bar)) : "memory");
-}
-
-// 16 TMEM lanes x 8 f32 columns -> the m16n8 accumulator fragment: lane
-// (r4, c) gets (lane r4, columns 2c, 2c+1) and (lane r4 + 8, same columns).
-// NT such loads at column offsets 0, 8, ..., then the wait; the registers
-// pass through the wait so that no use can be scheduled before it.
-template <int NT>
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[4 * NT]) {
-  static_assert(NT == 1 || NT == 2, "one or two column groups");
-  uint32_t r[4 * NT];
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[4 * t]), "=r"(r[4 * t + 1]), "=r"(r[4 * t + 2]), "=r"(r[4 * t + 3])
-                 : "r"(taddr + 8 * t) : "memory");
-  if (NT == 1)
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]) :: "memory");
-  else
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]),
-                   "+r"(r[4 * NT - 4]), "+r"(r[4 * NT - 3]), "+r"(r[4 * NT - 2]), "+r"(r[4 * NT - 1])
-                 :: "memory");
-#pragma unroll
-  for (int i = 0; i < 4 * NT; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 1/x for x a positive normal power of two, exactly, without a division.
@@ -323,20 +174,17 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   // shared array itself, so that every access below stays a shared-memory
   // access the compiler can tell apart from global memory
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  float* comb = reinterpret_cast<float*>(smem);
-  uint8_t* qtile = smem + C::kOffQ;                                       // [2] q slots
-  uint8_t* ring = smem + C::kOffRing;
-  int2* plist = reinterpret_cast<int2*>(smem + C::kOffPlist);
-  int4* meta = reinterpret_cast<int4*>(smem + C::kOffMeta);              // [NST]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint8_t* ring = smem;
+  float* comb = reinterpret_cast<float*>(smem + NST * C::kStageBytes);
+  int2* plist = reinterpret_cast<int2*>(smem + NST * C::kStageBytes + C::kCombineBytes);
+  int4* meta = reinterpret_cast<int4*>(plist + kWindow);                  // [NST]
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + NST);
   uint64_t* empty = full + NST;
-  uint64_t* sfull = empty + NST;           // the stage's QK MMAs are done: S^T in TMEM
-  uint64_t* cfull = sfull + NST;           // the consumers' states are in comb
+  uint64_t* cfull = empty + NST;           // the consumers' states are in comb
   uint64_t* cfree = cfull + 1;             // the merge warp is done reading comb
   uint64_t* cbar = cfree + 1;              // the consumer warps' barrier (last piece)
   __shared__ int s_abort;
   __shared__ int s_last;
-  __shared__ uint32_t s_tmem;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
@@ -345,7 +193,6 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
-      mbar_init(&sfull[i], 1);
     }
     mbar_init(cfull, kConsumerWarps);
     mbar_init(cfree, 1);
@@ -374,12 +221,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                                  : (const void*)(p.tickets + u_first);
     if (lane < 8) prefetch_l2(pf);
   }
-  // TMEM for the scores: kDCols columns per stage (the MMA warp allocates
-  // and frees it)
-  if (warp == kMmaWarp) tmem_alloc(&s_tmem, C::kTmemCols);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
   pdl_trigger();
   pdl_wait();                 // sel, phys, q and the pool come from earlier kernels
 
@@ -502,64 +344,6 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     return;
   }
 
-  if (warp == kMmaWarp) {
-    // ---------------- MMA warp -----------------------------------------------
-    // Lane 0 issues the QK MMAs of each stage as soon as its data has landed,
-    // in stage order, and commits them to the stage's sfull barrier; a stage
-    // without data gets a plain arrival, so that sfull counts the ring's
-    // phases and the consumers, who wait for it on every stage, never release
-    // a stage this warp has not read.  A page below 64 tokens starts
-    // 16 * ((pc * kBlocks) & 3) rows early so that its blocks land on the
-    // TMEM lanes of the warps that take them (pc: data pages so far).
-    const uint32_t tmem = s_tmem;
-    if (lane == 0) {
-      int pc = 0, n_st = 0;
-      for (int st = 0;; ++st) {
-        const int s2 = st % NST;
-        if (!mbar_wait(&full[s2], (st / NST) & 1, &s_abort)) {
-          s_abort = 1;
-          set_status(p.status, SSA_ST_TIMEOUT);
-          break;
-        }
-        const int4 d2 = meta[s2];
-        if (d2.x & kDone) break;
-        n_st = st + 1;
-        if (d2.x & kEmpty) {
-          mbar_arrive(&sfull[s2]);
-          continue;
-        }
-        tc_fence_after();
-        const int row0 = P < 64 ? 16 * ((pc * C::kBlocks) & 3) : 0;
-        const uint32_t kt = smem_u32(ring + s2 * C::kStageBytes) - row0 * 128;
-        const uint32_t qt = smem_u32(qtile + (d2.w & 1) * C::kQTileBytes);
-#pragma unroll
-        for (int hf = 0; hf < C::kHalves; ++hf) {
-          const uint32_t dcol = tmem + s2 * C::kDCols + hf * C::kNCols;
-#pragma unroll
-          for (int ks = 0; ks < (FP8 ? 4 : 8); ++ks) {        // 32 bytes of K per MMA
-            const int sl = FP8 ? 0 : ks >> 2;
-            const uint32_t off = 32 * (ks & 3);
-            const uint64_t ad = sw128_desc(kt + sl * P * 128 + hf * 64 * 128 + off);
-            const uint64_t bd = sw128_desc(qt + sl * 2048 + off);
-            tc_mma<FP8>(dcol, ad, bd, ks > 0);
-          }
-        }
-        tc_commit(&sfull[s2]);
-        ++pc;
-      }
-      // TMEM goes back only once every commit has arrived (the consumers
-      // waited for each; after an abort this bounded wait covers the rest)
-      for (int s3 = n_st > NST ? n_st - NST : 0; s3 < n_st; ++s3)
-        mbar_wait(&sfull[s3 % NST], (s3 / NST) & 1, nullptr);
-    }
-    __syncwarp();
-    tc_fence_before();
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers + 32) : "memory");   // consumers done with TMEM
-    tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
-    return;
-  }
-
   if (warp == kProducerWarp) {
     // ---------------- producer warp ----------------------------------------
     // The warp reads and compacts the rows; lane 0 alone issues the copies.
@@ -580,108 +364,19 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       return true;
     };
 
-    // q of a unit -> the QK B operand (Cfg::kQTileBytes).  fp8: lane (g4 =
-    // lane >> 3, j = lane & 7) takes d 16j..16j+15 of heads g4 and g4 + 4;
-    // bf16: 16-byte chunk i = lane + 32k is slab i >> 6, head (i >> 3) & 7,
-    // d 64 (i >> 6) + 8 (i & 7)..+7.  Heads >= G are zero.
-    uint4 qraw[4];
-    auto q_fetch = [&](int unit) {                        // all lanes
-      const uint4* qg = reinterpret_cast<const uint4*>(p.q + (size_t)unit * p.G * kD);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        int g, off;                                       // head, 16-byte word in its row
-        if (FP8) {
-          g = (lane >> 3) + 4 * (k >> 1);
-          off = 2 * (lane & 7) + (k & 1);
-        } else {
-          const int i = lane + 32 * k;
-          g = (i >> 3) & 7;
-          off = 8 * (i >> 6) + (i & 7);
-        }
-        qraw[k] = g < p.G ? qg[g * (kD / 8) + off] : make_uint4(0u, 0u, 0u, 0u);
-      }
-    };
-    // writes the tile of qraw into slot `slot`; returns the fp8 exponent eq
-    // (q * 2^eq has its largest magnitude in [128, 256) and is split into two
-    // e4m3 terms hi + lo, exact to 2^-10 of it, so QK runs on the raw K codes)
-    auto q_build = [&](int slot) -> int {                 // all lanes
-      uint8_t* qt = qtile + slot * C::kQTileBytes;
-      int eq = 0;
-      if (FP8) {
-        float amax = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) amax = fmaxf(amax, bf16x8_absmax(qraw[k]));
-        amax = warp_max(amax);
-        if (amax > 0.0f) {
-          const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);  // amax in [2^(ef-127), 2^(ef-126))
-          eq = 134 - ef;
-          eq = eq > 126 ? 126 : (eq < -126 ? -126 : eq);
-        }
-        const float up = __uint_as_float((uint32_t)(eq + 127) << 23);
-        const int j = lane & 7;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int g = (lane >> 3) + 4 * hh;
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const uint4 w = qraw[2 * hh + k];
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              const uint32_t a = ww[2 * m], b = ww[2 * m + 1];
-              const float x0 = __uint_as_float(a << 16) * up, x1 = __uint_as_float(a & 0xFFFF0000u) * up;
-              const float x2 = __uint_as_float(b << 16) * up, x3 = __uint_as_float(b & 0xFFFF0000u) * up;
-              const uint32_t H = f32x4_to_e4m3x4(x0, x1, x2, x3);
-              float y0, y1, y2, y3;
-              e4m3x4_to_f32x4(H, y0, y1, y2, y3);
-              hi[2 * k + m] = H;
-              lo[2 * k + m] = f32x4_to_e4m3x4(x0 - y0, x1 - y1, x2 - y2, x3 - y3);
-            }
-          }
-          *reinterpret_cast<uint4*>(qt + g * 128 + ((j ^ g) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(qt + (g + 8) * 128 + ((j ^ g) << 4)) =
-              make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = lane + 32 * k, sl = i >> 6, g = (i >> 3) & 7, cc = i & 7;
-          *reinterpret_cast<uint4*>(qt + sl * 2048 + g * 128 + ((cc ^ g) << 4)) = qraw[k];
-          *reinterpret_cast<uint4*>(qt + sl * 2048 + (g + 8) * 128 + ((cc ^ g) << 4)) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      // the tensor cores read the tile through the async proxy
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      return eq;
-    };
-    int n_built = 0;                  // q tiles built (slot = n_built & 1)
-    int slot_last0 = -1, slot_last1 = -1;   // lane 0: last stage index that read each slot
-
-    // lane 0: one page of K and V (one KV head) and its fp8 scales; qinfo =
-    // q slot | (eq + 256) << 1
-    auto issue_page = [&](int2 ent, int flags, int unit, int h, int layer, int seq_len,
-                          int qinfo) -> bool {
+    // lane 0: one page of K and V (one KV head), its fp8 scales and, on the
+    // first page of a piece, the unit's q rows
+    auto issue_page = [&](int2 ent, int flags, int unit, int h, int layer, int seq_len) -> bool {
       if (!acquire(st)) return false;
       const int sb = st % NST;
       const int nvalid = max(0, min(P, seq_len - ent.x * P));
-      meta[sb] = make_int4(flags, nvalid, unit, qinfo);
+      meta[sb] = make_int4(flags, nvalid, unit, 0);
       uint8_t* stage = ring + sb * C::kStageBytes;
-      mbar_arrive_expect_tx(&full[sb], 2 * C::kTileBytes + C::kScaleBytes);
+      const uint32_t qbytes = (flags & kFirst) ? (uint32_t)p.G * kD * 2 : 0u;
+      mbar_arrive_expect_tx(&full[sb], 2 * C::kTileBytes + C::kScaleBytes + qbytes);
       const int row_k = ((layer * p.S + ent.y) * p.Hkv + h) * P;
       if (FP8) {
-        if (p.k5d) {
-          tma_load_5d(stage, &tmK, &full[sb], 0, 0, 0, 0, row_k / 16);
-        } else {
-#pragma unroll
-          for (int blk = 0; blk < C::kBlocks; ++blk)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-              tma_load_3d(stage + (16 * blk + 8 * hh) * 128, &tmK, &full[sb], 0, 2 * hh,
-                          row_k / 4 + 4 * blk);
-        }
+        tma_load_2d(stage, &tmK, &full[sb], 0, row_k);
         const int row_v = ((layer * p.S + ent.y) * p.Hkv + h) * kD;
         tma_load_2d(stage + C::kTileBytes, &tmV, &full[sb], 0, row_v);
         const size_t so = ((size_t)layer * p.S + ent.y) * P;
@@ -693,11 +388,10 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         tma_load_2d(stage + C::kTileBytes, &tmV, &full[sb], 0, row_k);
         tma_load_2d(stage + C::kTileBytes + P * 128, &tmV, &full[sb], 64, row_k);
       }
+      if (qbytes) bulk_load(stage + C::kQOff, p.q + (size_t)unit * p.G * kD, qbytes, &full[sb]);
       ++st;
       return true;
     };
-
-    q_fetch(u_first);
 
     for (int u = u_first; u <= u_last && ok; ++u) {
       const int us = u * p.w;
@@ -735,24 +429,10 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       // this piece's share [a, e) of the unit's weight, as valid entries [j0, j1)
       const int j0 = (int)((long long)a * cnt / p.w), j1 = (int)((long long)e * cnt / p.w);
       if (j0 == j1) {
-        if (u < u_last) q_fetch(u + 1);
         if (lane == 0) ok = issue_marker(kEmpty | (u == u_last ? kFinal : 0), u);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         continue;
       }
-      // the q slot: the unit that used it before must be done with it, i.e.
-      // the consumers released its last page (they wait for a page's MMAs
-      // before they use it); the ring's own waits often show that already
-      const int slot = n_built & 1;
-      const int jl = slot ? slot_last1 : slot_last0;
-      if (lane == 0 && jl >= 0 && st <= jl + NST)
-        ok = mbar_wait(&empty[jl % NST], (jl / NST) & 1, &s_abort);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const int eq = q_build(slot);
-      const int qinfo = slot | ((eq + 256) << 1);
-      ++n_built;
-      if (u < u_last) q_fetch(u + 1);
       int seen = 0, issued = 0;
       for (int base = 0; base < p.W && seen < j1 && ok; base += 4 * 32) {
         int pgv[4], slv[4];
@@ -778,7 +458,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             for (int x = 0; x < nw && ok; ++x, ++issued) {
               const int flags = (issued == 0 ? kFirst : 0) |
                                 (issued == j1 - j0 - 1 ? (u == u_last ? kLast | kFinal : kLast) : 0);
-              ok = issue_page(plist[x], flags, u, h, layer, seq_len, qinfo);
+              ok = issue_page(plist[x], flags, u, h, layer, seq_len);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -786,8 +466,6 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           seen += __popc(m);
         }
       }
-      if (slot) slot_last1 = st - 1;
-      else slot_last0 = st - 1;
     }
     if (lane != 0) return;
     if (ok) ok = issue_marker(kDone, 0);
@@ -802,14 +480,12 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   }
 
   // ---------------- consumers -------------------------------------------------
-  // QK^T: tcgen05 MMAs, M = 64 (A = the page's K rows, tokens), N = 16
-  //       (B = the q tile), S^T[token][column] in TMEM; a warp reads the 16
-  //       lanes of its 16-token block as the m16n8 fragment.
-  // PV:   A = V^T rows (16 of d), B = P^T (S^T transposed in registers by
-  //       movmatrix), C = O^T[d][head], warp-level MMAs.
+  // QK^T: A = 16 K rows (tokens), B = q^T (8 heads), C = S^T[token][head].
+  // PV:   A = V^T rows (16 of d), B = P^T (C transposed in registers by
+  //       movmatrix), C = O^T[d][head].  No MMA row is padding.
   const int r4 = lane >> 2, c = lane & 3;
-  const uint32_t tmem_w = s_tmem + ((uint32_t)(32 * warp) << 16);   // this warp's TMEM lanes
 
+  uint32_t qb[8][2];
   float qscale_log2 = p.sm_log2;
   float o[8][4];   // O^T: rows d = 16*mt + r4 (+8), columns (heads) 2c, 2c+1
   // softmax state of heads 2c, 2c+1 (the lanes that own those O^T columns);
@@ -824,6 +500,17 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     vref = FP8 ? 0.0f : 1.0f;
   };
   reset();
+  const int rot = c >= 2 ? 16 : 0;      // fp8 V: lanes 2, 3 hold the token pairs swapped
+  // token of MMA row r4 and r4+8 within a 16-token block.  fp8: rows 2j, 2j+1
+  // and 2j+8, 2j+9 cover the 4 consecutive tokens 4j..4j+3 that one 32-bit V
+  // read returns, lanes of j >= 2 taking the pairs swapped so that the 8 rows
+  // one K read touches fall in distinct swizzle chunks (no bank conflicts)
+  int tauA = r4, tauB = r4 + 8;
+  if (FP8) {
+    const int j = r4 >> 1, e = r4 & 1;
+    tauA = 4 * j + (j < 2 ? e : 2 + e);
+    tauB = 4 * j + (j < 2 ? 2 + e : e);
+  }
 
   // End of a piece: leave this warp's state in comb for the merge warp
   // (once it has read the previous piece's) and stream on.  The consumer
@@ -1014,13 +701,6 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       }
       const int4 dsc = meta[sb];
       if (dsc.x & kDone) break;
-      // the MMA warp is through with the stage (data: S^T is in TMEM)
-      if (!mbar_wait(&sfull[sb], (st / NST) & 1, &s_abort)) {
-        s_abort = 1;
-        set_status(p.status, SSA_ST_TIMEOUT);
-        break;
-      }
-      tc_fence_after();
       if (dsc.x & kEmpty) {
         if (lane == 0) mbar_arrive(&empty[sb]);
         fkind = (dsc.x & kFinal) ? 2 : 1;
@@ -1029,70 +709,150 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       }
       const int nvalid = dsc.y;
       uint8_t* stage = ring + sb * C::kStageBytes;
-      const uint32_t vb = smem_u32(stage) + C::kTileBytes;
+      const uint32_t kb = smem_u32(stage);
+      const uint32_t vb = kb + C::kTileBytes;
       const float* ksc = reinterpret_cast<const float*>(stage + 2 * C::kTileBytes);
       const float* vsc = ksc + P;
-      // fp8: the MMAs saw q * 2^eq
-      if (FP8) qscale_log2 = p.sm_log2 * __uint_as_float((uint32_t)(127 - ((dsc.w >> 1) - 256)) << 23);
 
-      constexpr int kSteps = C::kBlocks;
+      if (dsc.x & kFirst) {
+        // the unit's G query rows as the B operand (rows >= G are zero).
+        // bf16: b0 = q[r4][k 2c, 2c+1], b1 = q[r4][k 2c+8, 2c+9] per k16 step.
+        // fp8: q * 2^eq as two e4m3 terms hi + lo (the top and the next four
+        // significant bits: their sum is q * 2^eq to within 2^-10, i.e.
+        // ~2^-18 of |q|max), so QK runs as e4m3 MMAs on the raw K codes;
+        // per k32 step b0 = d 32ks + 4c..+3, b1 = d + 16; qb[ks] = hi,
+        // qb[4 + ks] = lo
+        const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(stage + C::kQOff);
+        const bool row_ok = r4 < p.G;
+        if (FP8) {
+          float amax = 0.0f;
+          for (int i = lane; i < p.G * (kD / 8); i += 32)
+            amax = fmaxf(amax, bf16x8_absmax(*reinterpret_cast<const uint4*>(qs + i * 8)));
+          amax = warp_max(amax);
+          int eq = 0;
+          if (amax > 0.0f) {
+            const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);   // amax in [2^(ef-127), 2^(ef-126))
+            eq = 134 - ef;                                                // amax * 2^eq in [128, 256)
+            eq = eq > 126 ? 126 : (eq < -126 ? -126 : eq);
+          }
+          const float up = exp2f((float)eq);
+          qscale_log2 = p.sm_log2 * exp2f((float)-eq);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const __nv_bfloat16* r = qs + r4 * kD + 32 * ks + 16 * half + 4 * c;
+              float x[4], y[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) x[i] = row_ok ? __bfloat162float(r[i]) * up : 0.0f;
+              const uint32_t hi = f32x4_to_e4m3x4(x[0], x[1], x[2], x[3]);
+              e4m3x4_to_f32x4(hi, y[0], y[1], y[2], y[3]);
+              qb[ks][half] = hi;
+              qb[4 + ks][half] = f32x4_to_e4m3x4(x[0] - y[0], x[1] - y[1], x[2] - y[2], x[3] - y[3]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            qb[ks][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c) : 0u;
+            qb[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c + 8) : 0u;
+          }
+        }
+      }
+
+      // NB 16-token blocks per warp step share one softmax update (max,
+      // rescale, V-scale reference) and interleave their MMA chains.  Two per
+      // step measured no faster than one on GB300 and needs more registers
+      // than two CTAs per SM leave, so one.
+      constexpr int NB = 1;
+      constexpr int kSteps = C::kBlocks / NB;
 #pragma unroll 1
       for (int bs = 0; bs < kSteps; ++bs) {
         if (((pc * kSteps + bs) & (kConsumerWarps - 1)) != warp) continue;
-        const int tb = bs * 16;
+        const int tb0 = bs * NB * 16;
         // zero V of the tokens past seq_len (their bytes are not ours to trust)
-        if (nvalid < tb + 16) {
-          if (FP8) {
-            for (int i = lane; i < kD * 16; i += 32) {
-              const int d = i >> 4, xx = tb + (i & 15);
-              if (xx >= nvalid) stage[C::kTileBytes + swz(d * P + xx, C::kVSwz)] = 0;
-            }
-          } else {
-            for (int i = lane; i < 16 * 16; i += 32) {
-              const int r = tb + (i >> 4), ch = i & 15;
-              if (r >= nvalid)
-                *reinterpret_cast<uint4*>(stage + C::kTileBytes + (ch >> 3) * (P * 128) +
-                                          r * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+        if (nvalid < tb0 + NB * 16) {
+          for (int j = 0; j < NB; ++j) {
+            const int tb = tb0 + 16 * j;
+            if (nvalid >= tb + 16) continue;
+            if (FP8) {
+              for (int i = lane; i < kD * 16; i += 32) {
+                const int d = i >> 4, xx = tb + (i & 15);
+                if (xx >= nvalid) stage[C::kTileBytes + swz(d * P + xx, C::kVSwz)] = 0;
+              }
+            } else {
+              for (int i = lane; i < 16 * 16; i += 32) {
+                const int r = tb + (i >> 4), ch = i & 15;
+                if (r >= nvalid)
+                  *reinterpret_cast<uint4*>(stage + C::kTileBytes + (ch >> 3) * (P * 128) +
+                                            r * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+              }
             }
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
         }
-        // S^T of the block from TMEM: x[0], x[1] = token tkA, heads 2c, 2c+1;
-        // x[2], x[3] = token tkB (fp8: the hi and lo columns summed).  fp8 K
-        // rows arrive permuted (MMA row 8h + 2j + e = token 4j + 2h + e of the
-        // block), so that MMA rows 2c, 2c+1, 2c+8, 2c+9 -- the k indices of
-        // one lane's PV A operand -- are the 4 consecutive tokens 4c..4c+3.
-        const int tkA = FP8 ? tb + 4 * (r4 >> 1) + (r4 & 1) : tb + r4;
-        const int tkB = FP8 ? tkA + 2 : tb + r4 + 8;
-        float x[4];
-        {
-          const uint32_t ta = tmem_w + sb * C::kDCols + (P == 128 ? (bs >> 2) * C::kNCols : 0);
+
+        // S^T = K q^T per block; rows: x[j][0], x[j][1] = token tkA[j], heads
+        // 2c, 2c+1; x[j][2], x[j][3] = token tkB[j]
+        float x[NB][4], vsA[NB], vsB[NB];
+        int tkA[NB], tkB[NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          const int tb = tb0 + 16 * j;
+          float s4[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
+          tkA[j] = tb + tauA;
+          tkB[j] = tb + tauB;
           if (FP8) {
-            float v[8];
-            tmem_ld16<2>(ta, v);
+            // A = the K codes as they are: a0/a2 = token tkA, d 32ks + 4c..+3
+            // and d + 16; a1/a3 = token tkB.  hi and lo terms in two chains.
+            const uint32_t rA = kb + tkA[j] * 128 + 4 * c, rB = kb + tkB[j] * 128 + 4 * c;
+            const int xA = tkA[j] & 7, xB = tkB[j] & 7;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] = (v[i] + v[4 + i]) * qscale_log2;
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t a0 = lds32(rA + (((2 * ks) ^ xA) << 4));
+              const uint32_t a1 = lds32(rB + (((2 * ks) ^ xB) << 4));
+              const uint32_t a2 = lds32(rA + (((2 * ks + 1) ^ xA) << 4));
+              const uint32_t a3 = lds32(rB + (((2 * ks + 1) ^ xB) << 4));
+              mma_e4m3(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              mma_e4m3(sx, a0, a1, a2, a3, qb[4 + ks][0], qb[4 + ks][1]);
+            }
           } else {
-            float v[4];
-            tmem_ld16<1>(ta, v);
+            const int mi = lane >> 3, rr = lane & 7;
+            const int t = tb + (mi & 1) * 8 + rr;
+            const uint32_t rowk = kb + t * 128;
+            const int xt = t & 7;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] = v[i] * qscale_log2;
+            for (int ks = 0; ks < 8; ks += 2) {
+              uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+              const int c0 = 2 * ks + (mi >> 1), c1 = c0 + 2;     // 16-byte chunks over d
+              ldsm_x4(a0, a1, a2, a3, rowk + (c0 >> 3) * (P * 128) + (((c0 & 7) ^ xt) << 4));
+              ldsm_x4(a4, a5, a6, a7, rowk + (c1 >> 3) * (P * 128) + (((c1 & 7) ^ xt) << 4));
+              mma_bf16(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              mma_bf16(sx, a4, a5, a6, a7, qb[ks + 1][0], qb[ks + 1][1]);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) x[j][i] = (s4[i] + sx[i]) * qscale_log2;
+          vsA[j] = vsB[j] = 0.0f;
+          if (FP8) {
+            const float kA = ksc[tkA[j]], kB = ksc[tkB[j]];
+            x[j][0] *= kA; x[j][1] *= kA; x[j][2] *= kB; x[j][3] *= kB;
+            vsA[j] = vsc[tkA[j]];
+            vsB[j] = vsc[tkB[j]];
+          }
+          if (nvalid < tb + 16) {          // the tail of a request's last page
+            if (tkA[j] >= nvalid) { x[j][0] = x[j][1] = -INFINITY; vsA[j] = 0.0f; }
+            if (tkB[j] >= nvalid) { x[j][2] = x[j][3] = -INFINITY; vsB[j] = 0.0f; }
           }
         }
-        float vsA = 0.0f, vsB = 0.0f;
-        if (FP8) {
-          const float kA = ksc[tkA], kB = ksc[tkB];
-          x[0] *= kA; x[1] *= kA; x[2] *= kB; x[3] *= kB;
-          vsA = vsc[tkA];
-          vsB = vsc[tkB];
+        // per-head maxima over the step's tokens: the 8 lanes r4 = 0..7 of c
+        float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+        for (int j = 1; j < NB; ++j) {
+          mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][2]));
+          mx1 = fmaxf(mx1, fmaxf(x[j][1], x[j][3]));
         }
-        if (nvalid < tb + 16) {            // the tail of a request's last page
-          if (tkA >= nvalid) { x[0] = x[1] = -INFINITY; vsA = 0.0f; }
-          if (tkB >= nvalid) { x[2] = x[3] = -INFINITY; vsB = 0.0f; }
-        }
-        // per-head maxima over the block's tokens: the 8 lanes r4 = 0..7 of c
-        float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -1104,7 +864,9 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
         float oc0 = corr0, oc1 = corr1;
         float vinv = 1.0f;
         if (FP8) {
-          float vmax = fmaxf(vsA, vsB);
+          float vmax = fmaxf(vsA[0], vsB[0]);
+#pragma unroll
+          for (int j = 1; j < NB; ++j) vmax = fmaxf(vmax, fmaxf(vsA[j], vsB[j]));
 #pragma unroll
           for (int off = 4; off < 32; off <<= 1)
             vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
@@ -1117,30 +879,30 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           }
           vinv = pow2_rcp(vref);
         }
-        uint32_t b0, b1;
-        float ls0, ls1;
-        {
-          const float p0 = fast_exp2(x[0] - mu0), p1 = fast_exp2(x[1] - mu1);
-          const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
+        uint32_t b0[NB], b1[NB];
+        float ls0 = 0.0f, ls1 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          const float p0 = fast_exp2(x[j][0] - mu0), p1 = fast_exp2(x[j][1] - mu1);
+          const float p2 = fast_exp2(x[j][2] - mu0), p3 = fast_exp2(x[j][3] - mu1);
           uint32_t P0, P1;
           if (FP8) {
-            ls0 = p0 + p2;
-            ls1 = p1 + p3;
-            const float wA = vsA * vinv, wB = vsB * vinv;
+            ls0 += p0 + p2;
+            ls1 += p1 + p3;
+            const float wA = vsA[j] * vinv, wB = vsB[j] * vinv;
             P0 = pack_f16(p0 * wA, p1 * wA);
             P1 = pack_f16(p2 * wB, p3 * wB);
           } else {
             const float q0 = bf16_round(p0), q1 = bf16_round(p1);
             const float q2 = bf16_round(p2), q3 = bf16_round(p3);
-            ls0 = q0 + q2;
-            ls1 = q1 + q3;
+            ls0 += q0 + q2;
+            ls1 += q1 + q3;
             P0 = pack_bf16(q0, q1);
             P1 = pack_bf16(q2, q3);
           }
-          // P^T as the B operand: each 8x8 half transposed across the warp;
-          // b0 = MMA rows 2c, 2c+1, b1 = rows 2c+8, 2c+9, head r4
-          b0 = movmatrix_trans(P0);
-          b1 = movmatrix_trans(P1);
+          // P^T as the B operand: each 8x8 half transposed across the warp
+          b0[j] = movmatrix_trans(P0);
+          b1[j] = movmatrix_trans(P1);
         }
         l_run0 = l_run0 * corr0 + ls0;
         l_run1 = l_run1 * corr1 + ls1;
@@ -1153,36 +915,47 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           }
         }
 
-        // O^T += V^T P^T, 16 rows of d per MMA
+        // O^T += V^T P^T, 16 rows of d per MMA, the step's blocks in turn
         if (FP8) {
-          // A rows d = 16*mt + r4 and +8; k = 2c, 2c+1 (a0, a1) and 2c+8,
-          // 2c+9 (a2, a3) are tokens 4c..4c+3: one 32-bit read of the d-major
-          // V row.  The swizzle bits do not depend on mt (16*P*mt is a
-          // multiple of the swizzle period), so hoist them.
-          const uint32_t va0 = vb + swz(r4 * P + tb + 4 * c, C::kVSwz);
-          const uint32_t va1 = vb + swz((r4 + 8) * P + tb + 4 * c, C::kVSwz);
+          // rows d = 16*mt + r4 and +8: the swizzle bits do not depend on mt
+          // (16*P*mt is a multiple of the swizzle period), so hoist them
+          uint32_t va0[NB], va1[NB];
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            e4m3x4_to_f16x2x2(lds32(va0 + mt * 16 * P), a0, a2);
-            e4m3x4_to_f16x2x2(lds32(va1 + mt * 16 * P), a1, a3);
-            mma_f16(o[mt], a0, a1, a2, a3, b0, b1);
+          for (int j = 0; j < NB; ++j) {
+            va0[j] = vb + swz(r4 * P + tb0 + 16 * j + 4 * c, C::kVSwz);
+            va1[j] = vb + swz((r4 + 8) * P + tb0 + 16 * j + 4 * c, C::kVSwz);
+          }
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              uint32_t w0 = lds32(va0[j] + mt * 16 * P);
+              uint32_t w1 = lds32(va1[j] + mt * 16 * P);
+              w0 = __funnelshift_l(w0, w0, rot);
+              w1 = __funnelshift_l(w1, w1, rot);
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x2x2(w0, a0, a2);
+              e4m3x4_to_f16x2x2(w1, a1, a3);
+              mma_f16(o[mt], a0, a1, a2, a3, b0[j], b1[j]);
+            }
           }
         } else {
           const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
-            const int t = tb + (mi >> 1) * 8 + rr;
-            const int chunk = 2 * mt + (mi & 1);
-            const uint32_t addr =
-                vb + (chunk >> 3) * (P * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(a0, a1, a2, a3, addr);
-            mma_bf16(o[mt], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              const int t = tb0 + 16 * j + (mi >> 1) * 8 + rr;
+              const int chunk = 2 * mt + (mi & 1);
+              const uint32_t addr =
+                  vb + (chunk >> 3) * (P * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_t(a0, a1, a2, a3, addr);
+              mma_bf16(o[mt], a0, a1, a2, a3, b0[j], b1[j]);
+            }
           }
         }
       }
-      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[sb]);
       ++pc;
@@ -1195,10 +968,6 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     if (fkind == 1 && !flush()) break;
     if (fkind == 2 && !final_flush(funit)) break;
   }
-
-  // the MMA warp frees TMEM once the consumers are done reading it
-  tc_fence_before();
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers + 32) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -1229,68 +998,25 @@ bool make_tmap(CUtensorMap* tm, void* base, CUtensorMapDataType dt, int esz, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp8 K pages with their rows permuted within each 16-token block: shared
-// row 8h + 2j + e holds token 4j + 2h + e.  First choice, one box per page: a
-// 5-D view (128 bytes, e: 2, j: 4, h: 2, 16-token blocks) with the byte
-// strides 128, 512, 256, 2048.  If the driver will not encode that view, a
-// 3-D view (128 bytes, 4 rows, groups of 4 rows) with boxes of (128, 2, 4)
-// at row offset 2h: two boxes per block.
-bool make_tmap_kperm(CUtensorMap* tm, void* base, uint64_t rows, int P, int* k5d) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  {
-    cuuint64_t dims[5] = {(cuuint64_t)kD, 2, 4, 2, rows / 16};
-    cuuint64_t strides[4] = {128, 512, 256, 2048};
-    cuuint32_t box[5] = {(cuuint32_t)kD, 2, 4, 2, (cuuint32_t)(P / 16)};
-    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    if (fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, base, dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
-      *k5d = 1;
-      return true;
-    }
-  }
-  cuuint64_t dims[3] = {(cuuint64_t)kD, 4, rows / 4};
-  cuuint64_t strides[2] = {128, 512};
-  cuuint32_t box[3] = {(cuuint32_t)kD, 2, 4};
-  cuuint32_t estr[3] = {1, 1, 1};
-  *k5d = 0;
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <bool FP8, int P>
 size_t decode_smem() {
-  return (size_t)Cfg<FP8, P>::kSmemBytes;
+  using C = Cfg<FP8, P>;
+  return 1024 + (size_t)C::kStages * C::kStageBytes + C::kCombineBytes + kWindow * 8 +
+         (size_t)C::kStages * 16 + 2 * C::kStages * 8 + 4 * 8;
 }
 
 // CTAs of one wave: resident CTAs per SM (the configuration's target, or
-// what the kernel's registers and shared memory allow, whichever is lower)
-// x SMs, cut so that every CTA gets at least two tiles and no unit more
-// than 130 pieces.  (The runtime's occupancy calculator answers one CTA per
-// SM for this TMEM-allocating kernel although two fit and run together; the
-// TMEM budget is kept by construction, see Cfg::kTmemCols.)  No CTA waits
-// for another, so a wave that does not fit only runs longer.
+// what the occupancy calculator grants, whichever is lower) x SMs, cut so
+// that every CTA gets at least two tiles and no unit more than 130 pieces.
 template <bool FP8, int P>
 int decode_grid(const Dims& d, int n_layers, int num_sms) {
   static int occ = -1;
   if (occ < 0) {
-    int o = Cfg<FP8, P>::kCtasPerSm, dev = 0, regs_sm = 65536, smem_sm = kSmemPerSm;
-    cudaFuncAttributes fa{};
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaFuncGetAttributes(&fa, decode_kernel<FP8, P>) == cudaSuccess) {
-      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
-      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-      const int regs_cta = ((fa.numRegs * 32 + 255) / 256 * 256) * (kDecodeThreads / 32);
-      const int smem_cta = (int)(decode_smem<FP8, P>() + fa.sharedSizeBytes) + kSmemReservedPerCta;
-      const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : o;
-      const int by_smem = smem_cta > 0 ? smem_sm / smem_cta : o;
-      o = std::min(o, std::min(by_regs, by_smem));
-    } else {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<FP8, P>, kDecodeThreads,
+                                                      decode_smem<FP8, P>()) != cudaSuccess)
       o = 1;
-    }
-    occ = o < 1 ? 1 : o;
+    occ = o < 1 ? 1 : (o > Cfg<FP8, P>::kCtasPerSm ? Cfg<FP8, P>::kCtasPerSm : o);
   }
   const int w = d.max_selected();
   const long long T = (long long)n_layers * d.B * d.Hkv * w;
@@ -1308,7 +1034,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, DecodeParams& p, cudaStream_t s
   const uint64_t rows_tok = (uint64_t)d.Lyr * d.S * d.Hkv * P;
   bool ok;
   if (FP8) {
-    ok = make_tmap_kperm(&tmK, c.k_pool, rows_tok, P, &p.k5d);
+    ok = make_tmap(&tmK, c.k_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kD, rows_tok, kD, P,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
     const CUtensorMapSwizzle vsw = P >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                  : P == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
                                  : P == 32  ? CU_TENSOR_MAP_SWIZZLE_32B

@@ -515,6 +515,7 @@ def run_ours(args, rank: int, world: int, dist):
 
     if rank != 0:
         return None
+    store = time_store(w, run)
     peak, peak_kind = load_peaks()
     dec_ms = statistics.mean(stage_ms["decode"])
     dec_bytes = decode_bytes(w)
@@ -564,7 +565,61 @@ def run_ours(args, rank: int, world: int, dist):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    line["store"] = store
     return line, w
+
+
+def time_store(w: wl.Workload, run, chunk: int = 4096, n_append: int = 50):
+    """The store path on the filled cache, after every decode measurement:
+    the per-step append (one token per request, every layer in one call) and
+    a prefill chunk of `chunk` tokens per request (every layer in one call).
+    Positions already stored are stored again: the kernels do the same work
+    as on first store (the slab sums it leaves are not used afterwards)."""
+    import torch
+    L, B, P = w.n_layers, w.batch, w.page_size
+    bt = wl.block_table(w)
+    lens = w.lens.astype(np.int64)
+    g = torch.Generator(device="cuda").manual_seed(5)
+
+    def positions(tok):                     # tok[b]: token indices of request b
+        return torch.from_numpy(np.concatenate(
+            [bt[b][t // P].astype(np.int64) * P + t % P for b, t in enumerate(tok)])).cuda()
+
+    def kv(T):
+        shape = (L, T, w.n_kv_heads, w.head_dim)
+        return (torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16),
+                torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16))
+
+    def timed(k, v, pos, reps):
+        run.store(0, L, k, v, pos)          # warm
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run.store(0, L, k, v, pos)
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    mirror_per_tok = w.n_kv_heads * w.head_dim * 2 * (1 if w.fp8 else 2) + (8 if w.fp8 else 0)
+    k, v = kv(B)
+    app_ms = timed(k, v, positions([np.array([n - 1]) for n in lens]), n_append)
+    n_chunk = [np.arange(min(chunk, int(n))) for n in lens]
+    T = sum(len(t) for t in n_chunk)
+    k, v = kv(T)
+    pre_ms = timed(k, v, positions(n_chunk), 5)
+    torch.cuda.synchronize()
+    return {
+        "append": {"tokens_per_call": B, "layers_per_call": L, "us_per_call": 1e3 * app_ms,
+                   "calls_timed": n_append},
+        "prefill_chunk": {"tokens_per_request": chunk, "tokens_per_call": T, "layers_per_call": L,
+                          "ms_per_call": pre_ms, "tokens_per_s": T * L / (pre_ms * 1e-3),
+                          "mirror_write_gbs": T * L * mirror_per_tok / (pre_ms * 1e-3) / 1e9},
+        "note": "ssa_store_kv_mirror on the filled cache after the decode measurements; "
+                "positions stored again (same work as a first store)",
+    }
 
 
 def main():

@@ -39,6 +39,7 @@ struct StoreParams {
 };
 
 constexpr int kMaxPage = 128;
+constexpr int kMaxPerThread = 1;           // slab elements per thread: Hkv * D <= 1024 threads
 
 __device__ __forceinline__ uint8_t e4m3(float x) {
   return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
@@ -65,6 +66,16 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
     if (prev >= pos0 && tid == 0) set_status(p.status, SSA_ST_BAD_POS);
     if (prev >= 0 && prev / P == pg) return;          // not the first token of its run
   }
+  // the page's slab running sums and its slot, loaded now so that their
+  // latency overlaps the run-length scan; the sums stay in registers
+  const size_t so = ((size_t)layer * p.Lp + pg) * HD;
+  float sums[kMaxPerThread];
+#pragma unroll
+  for (int k = 0; k < kMaxPerThread; ++k) {
+    const int e = tid + k * (int)blockDim.x;
+    sums[k] = e < HD ? p.slab_sum[so + e] : 0.0f;
+  }
+  int slot = p.slot_of[(size_t)layer * p.Lp + pg];
   // run length: consecutive tokens of the same page (at most P)
   if (tid == 0) s_run = P;
   __syncthreads();
@@ -83,7 +94,6 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
   if (tid < R) s_j[tid] = (int)(p.pos[t0 + tid] % P);
   __syncthreads();
 
-  int slot = p.slot_of[(size_t)layer * p.Lp + pg];
   if (slot >= p.S) {                                    // corrupt state: never write through it
     if (tid == 0) set_status(p.status, SSA_ST_BAD_ID);
     slot = -1;
@@ -127,9 +137,12 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
 
   // phase 2: codes, mirror + pool writes, slab running sum (token order)
   const bool full_page = (R == P);
-  for (int e = tid; e < HD; e += blockDim.x) {
+#pragma unroll
+  for (int k = 0; k < kMaxPerThread; ++k) {
+    const int e = tid + k * (int)blockDim.x;
+    if (e >= HD) break;
     const int h = e / p.D, d = e - h * p.D;
-    float sum = p.slab_sum[((size_t)layer * p.Lp + pg) * HD + e];
+    float sum = sums[k];
     for (int r = 0; r < R; ++r) {
       const int j = s_j[r];
       const __nv_bfloat16 xk = kin[(size_t)r * HD + e];
@@ -155,7 +168,8 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
       }
       sum = sum + __bfloat162float(xk);
     }
-    p.slab_sum[((size_t)layer * p.Lp + pg) * HD + e] = sum;
+    sums[k] = sum;
+    p.slab_sum[so + e] = sum;
   }
   __syncthreads();
 
@@ -174,17 +188,19 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
   // phase 3b: re-quantise the page's slab row
   const int cnt = p.slab_cnt[(size_t)layer * p.Lp + pg] + R;
   float amax = 0.0f;
-  for (int e = tid; e < HD; e += blockDim.x) {
-    const float mean = p.slab_sum[((size_t)layer * p.Lp + pg) * HD + e] / (float)cnt;
-    amax = fmaxf(amax, fabsf(mean));
-  }
+#pragma unroll
+  for (int k = 0; k < kMaxPerThread; ++k)
+    if (tid + k * (int)blockDim.x < HD) amax = fmaxf(amax, fabsf(sums[k] / (float)cnt));
   amax = block_max(amax, red);
   const float s = amax / 127.0f;
-  for (int e = tid; e < HD; e += blockDim.x) {
-    const float mean = p.slab_sum[((size_t)layer * p.Lp + pg) * HD + e] / (float)cnt;
+#pragma unroll
+  for (int k = 0; k < kMaxPerThread; ++k) {
+    const int e = tid + k * (int)blockDim.x;
+    if (e >= HD) break;
+    const float mean = sums[k] / (float)cnt;
     int c = 0;
     if (amax > 0.0f) c = (int)fminf(fmaxf(rintf(mean / s), -127.0f), 127.0f);
-    p.slab[((size_t)layer * p.Lp + pg) * HD + e] = (int8_t)c;
+    p.slab[so + e] = (int8_t)c;
   }
   if (tid == 0) {
     p.slab_cnt[(size_t)layer * p.Lp + pg] = cnt;
@@ -250,6 +266,7 @@ cudaError_t launch_store(const Dims& d, const ssa_cache& c, int layer0, int n_la
   p.status = status;
   p.layer0 = layer0;
   p.Lp = d.Lp; p.S = d.S; p.Hkv = d.Hkv; p.D = d.D; p.P = d.P; p.fp8 = d.fp8;
+  if (d.Hkv * d.D > 1024 * kMaxPerThread) return cudaErrorInvalidValue;
   const int threads = d.Hkv * d.D > 1024 ? 1024 : d.Hkv * d.D;
   const size_t smem = d.fp8 ? (size_t)d.Hkv * d.D * d.P : 0;
   if (smem > 48 * 1024) {

@@ -171,6 +171,9 @@ int ssa_lru_init(const ssa_layout *lay, const ssa_cache *c, int identity,
  *   pos    [T] int64 logical token ids, page = pos / P, row j = pos % P;
  *          strictly increasing within the call (SSA_ST_BAD_POS otherwise),
  *          each position stored once over the cache's lifetime
+ * A call holds any run of tokens: a prefill chunk, or the one token per
+ * request a decode step appends; a page may be filled over many calls, and
+ * its slab row then equals that of one call storing the same tokens.
  * fp8: per token and tensor, s = max|x| / 448 over all KV heads (1 if the
  * token is all zero), code = e4m3(x / s) rounded to nearest even,
  * saturating.  Writes the mirror always (when present) and the pool slot

@@ -3,16 +3,16 @@
 Per request-layer the method must move the int8 slab of every page
 (n * (Hkv * D + 4)), the selected pages' K and V (n_sel * P * Hkv * D * 2
 bytes of codes, bf16 twice that), the fp8 per-token scales (n_sel * P * 8),
-and q, out, sel, phys.  The totals below are the per-request-layer and
-per-step figures of the survey's measurement table for the three fixed
-workloads.  The table rounds its own inputs (host_tier_196k_fp8 is printed as
-1.92 MB per request-layer; the count is 1.910), so the totals agree within
-1 %; the hand count below is exact.
+and q, out, sel, phys.  The totals below are those figures for the three
+fixed workloads as first worked out by hand, to 2-3 significant figures and
+from rounded inputs (host_tier_196k_fp8 came to 1.92 MB per request-layer;
+the exact count is 1.910), so they agree within 1 %; the hand count of the
+second test is exact.
 """
 import bench
 import workloads as wl
 
-# workload: (MB per request-layer, MB per step), as printed
+# workload: (MB per request-layer, MB per step), worked out by hand
 PRINTED = {
     "batched_32k_bf16_needles": (2.31, 110.7),
     "host_tier_196k_fp8": (1.92, 23.0),

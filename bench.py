@@ -525,6 +525,9 @@ def run_ours(args, rank: int, world: int, dist):
     miss_bytes = misses * page_fetch_bytes(w) / K
     stage_miss_bytes = int(stage_miss.sum().item()) * page_fetch_bytes(w) / K
     h2d = h2d_peak_gbs(torch)
+    # pages the step selects (every layer and request): those already bound
+    # are the ones the pool kept from earlier steps, fetched by no one now
+    sel_per_step = w.n_layers * int(n_selected(w).sum())
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": 1e3 * total_s / K, "higher_is_better": True,
@@ -549,6 +552,8 @@ def run_ours(args, rank: int, world: int, dist):
         "index_roofline": {"alg_bytes": index_bytes(w),
                            "achieved_gbs": index_bytes(w) / (idx_ms * 1e-3) / 1e9},
         "miss": {"pages_per_step": misses / K, "bytes_per_step": miss_bytes,
+                 "selected_pages_per_step": sel_per_step,
+                 "resident_fraction": 1.0 - (misses / K) / sel_per_step,
                  "gbs_over_ensure_stage": stage_miss_bytes / (ens_ms * 1e-3) / 1e9,
                  "h2d_copy_engine_peak_gbs": h2d,
                  "frac_of_h2d_peak": (stage_miss_bytes / (ens_ms * 1e-3) / 1e9 / h2d

@@ -104,3 +104,40 @@ def test_binding_refuses_to_run_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(m, "_lib", None)
     with pytest.raises(RuntimeError):
         m.lib()
+
+
+def test_more_host_side_rejections(L):
+    """The remaining documented host-side rejections, each before any launch."""
+    lib = L.lib()
+    p = ctypes.c_void_p(0x10000)
+    c = _fake_cache(L)
+    UNSUPPORTED, INVALID = -3, -1
+    # KV heads: a power of two, at most 8
+    for bad in (dict(n_q_heads=6, n_kv_heads=3), dict(n_q_heads=16, n_kv_heads=16)):
+        lay = _layout(L, **bad).c()
+        assert lib.ssa_workspace_size(ctypes.byref(lay)) == 0, bad
+        assert lib.ssa_store_kv_mirror(ctypes.byref(lay), ctypes.byref(c), 0, 1, p, p, p, 4, p,
+                                       None) == UNSUPPORTED, bad
+    # a batch selection the LRU cannot sort in shared memory: 256 * 72 > 16,384
+    lay = _layout(L, batch=256, logical_pages=25600, pool_slots=25600, max_pages=100).c()
+    assert lib.ssa_workspace_size(ctypes.byref(lay)) == 0
+    # more pages per request than the select keeps on chip
+    lay = _layout(L, logical_pages=50000, pool_slots=50000, max_pages=50000).c()
+    assert lib.ssa_workspace_size(ctypes.byref(lay)) == 0
+    lay = _layout(L).c()
+    # attention without its workspace
+    assert lib.ssa_sparse_paged_decode(ctypes.byref(lay), ctypes.byref(c), 0, 1, p, p, p, p,
+                                       0.088, p, p, None, None) == INVALID
+    # store: a negative token count, or tokens without their data
+    assert lib.ssa_store_kv_mirror(ctypes.byref(lay), ctypes.byref(c), 0, 1, p, p, p, -1, p,
+                                   None) == INVALID
+    assert lib.ssa_store_kv_mirror(ctypes.byref(lay), ctypes.byref(c), 0, 1, None, p, p, 4, p,
+                                   None) == INVALID
+    # ensure with neither a workspace nor the miss outputs
+    assert lib.ssa_ensure_resident(ctypes.byref(lay), ctypes.byref(c), 0, 1, p, p, None, None,
+                                   None, p, None, None) == INVALID
+    # an fp8 cache without its scale banks
+    c2 = _fake_cache(L)
+    c2.k_scale = None
+    assert lib.ssa_sparse_paged_decode(ctypes.byref(lay), ctypes.byref(c2), 0, 1, p, p, p, p,
+                                       0.088, p, p, p, None) == INVALID

@@ -3,8 +3,9 @@
 Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package.  The CUDA library never does, and this package
 never imports the library: the two share no code.  The arithmetic lives in
-``ssa_oracle.c`` (plain C, single-threaded, fp64 attention, built with
-``-O2 -ffp-contract=off``); this module only builds it, holds the oracle's own
+``ssa_oracle.c`` (plain C, fp64 attention, built with ``-O2
+-ffp-contract=off``; independent loops spread over the cores by OpenMP,
+with results independent of the thread count); this module only builds it, holds the oracle's own
 copy of the KV state in numpy arrays and marshals arguments.
 
 State layout per layer (the oracle's own, plain [P][D] for both K and V):
@@ -35,12 +36,17 @@ CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC", "-s
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (host architecture) if it is missing or stale."""
+    """Compile the oracle with gcc (host architecture) if it is missing or stale.
+    With OpenMP where the compiler has it (independent loops on every core;
+    the results are the same at any thread count), else single-threaded."""
     stale = (not os.path.exists(_LIB)) or any(
-        os.path.getmtime(p) > os.path.getmtime(_LIB) for p in (_SRC, _HDR))
+        os.path.getmtime(p) > os.path.getmtime(_LIB) for p in (_SRC, _HDR, __file__))
     if force or stale:
         tmp = _LIB + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+        r = subprocess.run(["gcc", *CFLAGS, "-fopenmp", _SRC, "-o", tmp, "-lm"],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -73,12 +79,26 @@ def _load():
         lib.or_remap.argtypes = [vp] * 5
         lib.or_decode.restype = None
         lib.or_decode.argtypes = [vp] * 9 + [ctypes.c_double, vp]
+        lib.or_set_threads.restype = None
+        lib.or_set_threads.argtypes = [i32]
+        lib.or_threads.restype = i32
+        lib.or_threads.argtypes = []
         _lib = lib
     return _lib
 
 
 def _p(a):
     return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def set_threads(n: int) -> None:
+    """Threads for the oracle's independent loops (n <= 0: every core).  The
+    results are the same at any count."""
+    _load().or_set_threads(int(n))
+
+
+def threads() -> int:
+    return int(_load().or_threads())
 
 
 def e4m3_encode(x: float) -> int:

@@ -1,5 +1,5 @@
 /*
- * ssa_oracle.c -- plain, slow, single-threaded CPU oracle for the per-layer
+ * ssa_oracle.c -- plain, slow CPU oracle for the per-layer
  * sparse-attention decode step: store through a write-through mirror, int8
  * indexer, top-k page selection, LRU ensure + miss copy, block-table remap,
  * exact attention over the selected pages.
@@ -8,6 +8,11 @@
  * baseline use it; the CUDA library never does.  It shares no code with the
  * library.  Built with -O2 -ffp-contract=off and no fast-math, so every fp32
  * operation below is one correctly rounded IEEE operation in program order.
+ * Loops whose iterations are independent (tokens of a store, pages of a
+ * score, requests of a selection, (request, head) outputs of the attention)
+ * carry OpenMP pragmas; each result is still computed by one thread in the
+ * order written, so the results do not depend on the thread count, and
+ * without OpenMP the pragmas are ignored.
  *
  * Sources (web pages, cited by title and section):
  *   [FT499]  FreeToken PR #499 "host-RAM KV tier for sparse-attention models
@@ -27,6 +32,9 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                           */
@@ -116,7 +124,10 @@ int or_store(const or_layout *L,
   const int HD = L->Hkv * L->D;
   const size_t esz = L->fp8 ? 1 : 2;
   int bad = 0;
-  char *touched = (char *)calloc((size_t)L->Lp, 1);
+  /* 1. each token's codes (and scale) into the mirror and, when resident, the
+   *    slot.  Tokens write disjoint bytes (positions are distinct), so the
+   *    loop runs its iterations in any order. */
+#pragma omp parallel for schedule(static) reduction(+ : bad)
   for (int t = 0; t < T; ++t) {
     int64_t page64 = pos[t] / L->P;
     if (pos[t] < 0 || page64 >= L->Lp) { ++bad; continue; }
@@ -157,36 +168,74 @@ int or_store(const or_layout *L,
         if (slot >= 0) psc[(size_t)slot * L->P + j] = s;
       }
     }
-    /* slab running sum, token order */
-    const uint16_t *xk = k + (size_t)t * HD;
-    float *sum = slab_sum + (size_t)page * HD;
-    for (int i = 0; i < HD; ++i) sum[i] = sum[i] + or_bf16_to_float(xk[i]);
-    slab_cnt[page] += 1;
-    touched[page] = 1;
   }
-  /* re-quantise every page this call touched */
-  float *mean = (float *)malloc(sizeof(float) * HD);
-  for (int page = 0; page < L->Lp; ++page) {
-    if (!touched[page]) continue;
-    const float *sum = slab_sum + (size_t)page * HD;
-    float cnt = (float)slab_cnt[page];
-    float amax = 0.0f;
-    for (int i = 0; i < HD; ++i) {
-      mean[i] = sum[i] / cnt;
-      if (fabsf(mean[i]) > amax) amax = fabsf(mean[i]);
-    }
-    float s = amax / 127.0f;
-    slab_scale[page] = s;
-    for (int i = 0; i < HD; ++i) {
-      int c = 0;
-      if (amax > 0.0f) {
-        float r = rintf(mean[i] / s);
-        c = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);
+  /* 2. slab running sums, in token order within each page.  With positions
+   *    increasing (the store contract) a page's tokens form one contiguous
+   *    run of the call: runs are independent and each is summed front to
+   *    back.  Otherwise every token is summed in call order, one by one. */
+  int *run0 = (int *)malloc(sizeof(int) * ((size_t)T + 1));
+  int nrun = 0, ordered = 1;
+  int64_t prev = -1;
+  for (int t = 0; t < T; ++t) {
+    if (pos[t] < 0 || pos[t] / L->P >= L->Lp) continue;
+    if (pos[t] <= prev) ordered = 0;
+    prev = pos[t];
+    if (nrun == 0 || pos[t] / L->P != pos[run0[nrun - 1]] / L->P) run0[nrun++] = t;
+  }
+  char *touched = (char *)calloc((size_t)L->Lp, 1);
+  if (ordered) {
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int r = 0; r < nrun; ++r) {
+      const int64_t page = pos[run0[r]] / L->P;
+      float *sum = slab_sum + (size_t)page * HD;
+      const int t1 = r + 1 < nrun ? run0[r + 1] : T;
+      for (int t = run0[r]; t < t1; ++t) {
+        if (pos[t] < 0 || pos[t] / L->P != page) continue;   /* out-of-range ids */
+        const uint16_t *xk = k + (size_t)t * HD;
+        for (int i = 0; i < HD; ++i) sum[i] = sum[i] + or_bf16_to_float(xk[i]);
+        slab_cnt[page] += 1;
       }
-      slab[(size_t)page * HD + i] = (int8_t)c;
+      touched[page] = 1;
+    }
+  } else {
+    for (int t = 0; t < T; ++t) {
+      if (pos[t] < 0 || pos[t] / L->P >= L->Lp) continue;
+      const int64_t page = pos[t] / L->P;
+      const uint16_t *xk = k + (size_t)t * HD;
+      float *sum = slab_sum + (size_t)page * HD;
+      for (int i = 0; i < HD; ++i) sum[i] = sum[i] + or_bf16_to_float(xk[i]);
+      slab_cnt[page] += 1;
+      touched[page] = 1;
     }
   }
-  free(mean);
+  free(run0);
+  /* 3. re-quantise every page this call touched (pages are independent) */
+#pragma omp parallel
+  {
+    float *mean = (float *)malloc(sizeof(float) * HD);
+#pragma omp for schedule(dynamic, 256)
+    for (int page = 0; page < L->Lp; ++page) {
+      if (!touched[page]) continue;
+      const float *sum = slab_sum + (size_t)page * HD;
+      float cnt = (float)slab_cnt[page];
+      float amax = 0.0f;
+      for (int i = 0; i < HD; ++i) {
+        mean[i] = sum[i] / cnt;
+        if (fabsf(mean[i]) > amax) amax = fabsf(mean[i]);
+      }
+      float s = amax / 127.0f;
+      slab_scale[page] = s;
+      for (int i = 0; i < HD; ++i) {
+        int c = 0;
+        if (amax > 0.0f) {
+          float r = rintf(mean[i] / s);
+          c = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);
+        }
+        slab[(size_t)page * HD + i] = (int8_t)c;
+      }
+    }
+    free(mean);
+  }
   free(touched);
   return bad;
 }
@@ -213,9 +262,10 @@ int or_index_scores(const or_layout *L, const int8_t *slab, const uint16_t *q,
                     const int32_t *bt, const int32_t *seq_lens, int32_t *scores) {
   const int G = L->Hq / L->Hkv, HQD = L->Hq * L->D;
   int bad = 0;
-  int32_t *q8 = (int32_t *)malloc(sizeof(int32_t) * HQD);
+  int32_t *q8 = (int32_t *)malloc(sizeof(int32_t) * (size_t)L->B * HQD);
   for (int b = 0; b < L->B; ++b) {
     const uint16_t *qb = q + (size_t)b * HQD;
+    int32_t *q8b = q8 + (size_t)b * HQD;
     float amax = 0.0f;
     for (int i = 0; i < HQD; ++i) {
       float a = fabsf(or_bf16_to_float(qb[i]));
@@ -228,22 +278,26 @@ int or_index_scores(const or_layout *L, const int8_t *slab, const uint16_t *q,
         float r = rintf(or_bf16_to_float(qb[i]) / s);
         c = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);
       }
-      q8[i] = c;
+      q8b[i] = c;
     }
-    int n = pages_of(L, seq_lens[b]);
-    for (int p = 0; p < L->n_max; ++p) {
-      int32_t *out = &scores[(size_t)b * L->n_max + p];
-      *out = INT32_MIN;
-      if (p >= n) continue;
-      int id = bt[(size_t)b * L->n_max + p];
-      if (id < 0 || id >= L->Lp) { ++bad; continue; }
-      int64_t acc = 0;
-      for (int hq = 0; hq < L->Hq; ++hq)
-        for (int d = 0; d < L->D; ++d)
-          acc += (int64_t)q8[hq * L->D + d] *
-                 (int64_t)slab[((size_t)id * L->Hkv + hq / G) * L->D + d];
-      *out = (int32_t)acc;
-    }
+  }
+  /* every score is its own exact integer sum: pages in any order */
+  const long long total = (long long)L->B * L->n_max;
+#pragma omp parallel for schedule(static) reduction(+ : bad)
+  for (long long bp = 0; bp < total; ++bp) {
+    const int b = (int)(bp / L->n_max), p = (int)(bp % L->n_max);
+    const int32_t *q8b = q8 + (size_t)b * HQD;
+    int32_t *out = &scores[bp];
+    *out = INT32_MIN;
+    if (p >= pages_of(L, seq_lens[b])) continue;
+    int id = bt[(size_t)b * L->n_max + p];
+    if (id < 0 || id >= L->Lp) { ++bad; continue; }
+    int64_t acc = 0;
+    for (int hq = 0; hq < L->Hq; ++hq)
+      for (int d = 0; d < L->D; ++d)
+        acc += (int64_t)q8b[hq * L->D + d] *
+               (int64_t)slab[((size_t)id * L->Hkv + hq / G) * L->D + d];
+    *out = (int32_t)acc;
   }
   free(q8);
   return bad;
@@ -278,33 +332,37 @@ static int int_cmp(const void *a, const void *b) {
 int or_select(const or_layout *L, const int32_t *scores, const int32_t *seq_lens,
               int32_t *sel, int32_t *n_sel) {
   int drops = 0;
-  cand *c = (cand *)malloc(sizeof(cand) * (L->n_max + 1));
-  int32_t *chosen = (int32_t *)malloc(sizeof(int32_t) * (L->n_max + 1));
-  for (int b = 0; b < L->B; ++b) {
-    int n = pages_of(L, seq_lens[b]);
-    int m = 0;
-    if (n > 0) {
-      if (n - 1 <= L->k) {
-        for (int p = 0; p < n; ++p) chosen[m++] = p;
-      } else {
-        for (int p = 0; p < n - 1; ++p) {
-          c[p].score = scores[(size_t)b * L->n_max + p];
-          c[p].page = p;
+#pragma omp parallel reduction(+ : drops)
+  {
+    cand *c = (cand *)malloc(sizeof(cand) * (L->n_max + 1));
+    int32_t *chosen = (int32_t *)malloc(sizeof(int32_t) * (L->n_max + 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int b = 0; b < L->B; ++b) {
+      int n = pages_of(L, seq_lens[b]);
+      int m = 0;
+      if (n > 0) {
+        if (n - 1 <= L->k) {
+          for (int p = 0; p < n; ++p) chosen[m++] = p;
+        } else {
+          for (int p = 0; p < n - 1; ++p) {
+            c[p].score = scores[(size_t)b * L->n_max + p];
+            c[p].page = p;
+          }
+          qsort(c, (size_t)(n - 1), sizeof(cand), cand_cmp);
+          for (int i = 0; i < L->k; ++i) chosen[m++] = c[i].page;
+          chosen[m++] = n - 1;
+          qsort(chosen, (size_t)m, sizeof(int32_t), int_cmp);
         }
-        qsort(c, (size_t)(n - 1), sizeof(cand), cand_cmp);
-        for (int i = 0; i < L->k; ++i) chosen[m++] = c[i].page;
-        chosen[m++] = n - 1;
-        qsort(chosen, (size_t)m, sizeof(int32_t), int_cmp);
       }
+      int kept = m < L->W ? m : L->W;
+      drops += m - kept;
+      for (int i = 0; i < L->W; ++i)
+        sel[(size_t)b * L->W + i] = i < kept ? chosen[i] : -1;
+      n_sel[b] = kept;
     }
-    int kept = m < L->W ? m : L->W;
-    drops += m - kept;
-    for (int i = 0; i < L->W; ++i)
-      sel[(size_t)b * L->W + i] = i < kept ? chosen[i] : -1;
-    n_sel[b] = kept;
+    free(chosen);
+    free(c);
   }
-  free(chosen);
-  free(c);
   return drops;
 }
 
@@ -457,25 +515,35 @@ void or_decode(const or_layout *L, const uint8_t *k_pool, const uint8_t *v_pool,
   const int G = L->Hq / L->Hkv, D = L->D;
   const size_t esz = L->fp8 ? 1 : 2;
   const size_t ntok_max = (size_t)L->W * L->P;
-  double *sc = (double *)malloc(sizeof(double) * ntok_max);
-  int32_t *tslot = (int32_t *)malloc(sizeof(int32_t) * ntok_max);
-  int32_t *tj = (int32_t *)malloc(sizeof(int32_t) * ntok_max);
-  double *qd = (double *)malloc(sizeof(double) * D);
+  /* the token list of every request: (slot, row) pairs in selection order */
+  int32_t *tslot = (int32_t *)malloc(sizeof(int32_t) * ntok_max * L->B);
+  int32_t *tj = (int32_t *)malloc(sizeof(int32_t) * ntok_max * L->B);
+  size_t *ntok = (size_t *)malloc(sizeof(size_t) * L->B);
   for (int b = 0; b < L->B; ++b) {
-    /* the token list of this request */
     size_t nt = 0;
     for (int i = 0; i < L->W; ++i) {
       int p = sel[(size_t)b * L->W + i], s = phys[(size_t)b * L->W + i];
       if (p < 0 || s < 0) continue;
       for (int j = 0; j < L->P; ++j) {
         if ((int64_t)p * L->P + j >= seq_lens[b]) break;
-        tslot[nt] = s;
-        tj[nt] = j;
+        tslot[b * ntok_max + nt] = s;
+        tj[b * ntok_max + nt] = j;
         ++nt;
       }
     }
-    for (int hq = 0; hq < L->Hq; ++hq) {
+    ntok[b] = nt;
+  }
+  /* every (request, query head) output is computed whole by one thread */
+#pragma omp parallel
+  {
+    double *sc = (double *)malloc(sizeof(double) * (ntok_max + 1));
+    double *qd = (double *)malloc(sizeof(double) * D);
+#pragma omp for schedule(dynamic, 1)
+    for (int bh = 0; bh < L->B * L->Hq; ++bh) {
+      const int b = bh / L->Hq, hq = bh % L->Hq;
       const int h = hq / G;
+      const size_t nt = ntok[b];
+      const int32_t *ts = tslot + b * ntok_max, *tjj = tj + b * ntok_max;
       double *o = out + ((size_t)b * L->Hq + hq) * D;
       for (int d = 0; d < D; ++d) {
         qd[d] = or_bf16_to_float(q[((size_t)b * L->Hq + hq) * D + d]);
@@ -484,13 +552,13 @@ void or_decode(const or_layout *L, const uint8_t *k_pool, const uint8_t *v_pool,
       if (nt == 0) continue;
       double mx = -INFINITY;
       for (size_t t = 0; t < nt; ++t) {
-        size_t base = ((size_t)tslot[t] * L->Hkv + h) * L->P + tj[t];
+        size_t base = ((size_t)ts[t] * L->Hkv + h) * L->P + tjj[t];
         double dot = 0.0;
         for (int d = 0; d < D; ++d) {
           double kv;
           if (L->fp8) {
             kv = or_e4m3_decode(k_pool[base * D + d]) *
-                 (double)k_scale[(size_t)tslot[t] * L->P + tj[t]];
+                 (double)k_scale[(size_t)ts[t] * L->P + tjj[t]];
           } else {
             uint16_t bits;
             memcpy(&bits, k_pool + (base * D + d) * esz, 2);
@@ -505,12 +573,12 @@ void or_decode(const or_layout *L, const uint8_t *k_pool, const uint8_t *v_pool,
       for (size_t t = 0; t < nt; ++t) {
         double w = exp(sc[t] - mx);
         l += w;
-        size_t base = ((size_t)tslot[t] * L->Hkv + h) * L->P + tj[t];
+        size_t base = ((size_t)ts[t] * L->Hkv + h) * L->P + tjj[t];
         for (int d = 0; d < D; ++d) {
           double vv;
           if (L->fp8) {
             vv = or_e4m3_decode(v_pool[base * D + d]) *
-                 (double)v_scale[(size_t)tslot[t] * L->P + tj[t]];
+                 (double)v_scale[(size_t)ts[t] * L->P + tjj[t]];
           } else {
             uint16_t bits;
             memcpy(&bits, v_pool + (base * D + d) * esz, 2);
@@ -521,9 +589,29 @@ void or_decode(const or_layout *L, const uint8_t *k_pool, const uint8_t *v_pool,
       }
       for (int d = 0; d < D; ++d) o[d] /= l;
     }
+    free(qd);
+    free(sc);
   }
-  free(qd);
+  free(ntok);
   free(tj);
   free(tslot);
-  free(sc);
+}
+
+/* Threads the parallel loops above may use (<= 0: the OpenMP default, every
+ * core).  Results do not depend on it: each output element is computed by
+ * one thread in a fixed order. */
+void or_set_threads(int n) {
+#ifdef _OPENMP
+  omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+  (void)n;
+#endif
+}
+
+int or_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
 }

@@ -86,4 +86,10 @@ void or_decode(const or_layout *L, const uint8_t *k_pool, const uint8_t *v_pool,
                const int32_t *sel, const int32_t *phys, const int32_t *seq_lens,
                double sm_scale, double *out);
 
+/* --- threads ------------------------------------------------------------ */
+/* Threads the independent loops may use (n <= 0: every core); results never
+ * depend on it.  or_threads: the count now in force (1 without OpenMP). */
+void or_set_threads(int n);
+int or_threads(void);
+
 #endif

@@ -8,9 +8,9 @@ on each side separately.
 
 Recipe (all draws: numpy PCG64 ``default_rng``, float32 N(0, 1), rounded to
 bf16 with round-to-nearest-even):
-  * K, V for layer l:  rng([seed, l, 1]); K drawn first, then V, shape
-    [B][T_max][Hkv][D] with T_max = pages_per_request * P.  Only the first
-    seq_len[b] tokens of request b are stored.
+  * K, V of request b in layer l:  rng([seed, l, 1, b]); K drawn first, then
+    V, shape [seq_len[b]][Hkv][D].  Requests have streams of their own, so
+    they are drawn in parallel threads with the same result.
   * queries for layer l: rng([seed, l, 2]); q_0 ~ N(0, 1) [B][Hq][D];
     q_t = rho * q_{t-1} + c * eps_t, kept in fp32 and rounded to bf16 per step.
   * needles: rng([seed, 3]) draws, per request, ``needles`` distinct pages from
@@ -182,21 +182,28 @@ def needle_pages(w: Workload) -> np.ndarray:
     return out
 
 
-def kv_f32(w: Workload, layer: int):
-    """K, V fp32 [B][T_max][Hkv][D] (needles planted in K)."""
-    rng = np.random.default_rng([w.seed, layer, 1])
-    T = w.pages_per_request * w.page_size
-    shape = (w.batch, T, w.n_kv_heads, w.head_dim)
+def _needle_dirs(w: Workload, layer: int) -> np.ndarray | None:
+    """[B][Hkv][D] unit directions of the needles (sum of each KV head's query
+    heads at step 0), or None without needles."""
+    if not w.needles:
+        return None
+    q0 = query_walk_f32(w.with_(steps=1), layer)[0]          # [B][Hq][D]
+    qh = q0.reshape(w.batch, w.n_kv_heads, w.group, w.head_dim).sum(axis=2)
+    return qh / np.linalg.norm(qh, axis=-1, keepdims=True)
+
+
+def kv_request_f32(w: Workload, layer: int, b: int, qh=None):
+    """K, V fp32 [seq_len[b]][Hkv][D] of request b (needles planted in K)."""
+    rng = np.random.default_rng([w.seed, layer, 1, b])
+    shape = (int(w.lens[b]), w.n_kv_heads, w.head_dim)
     k = rng.standard_normal(shape, dtype=np.float32)
     v = rng.standard_normal(shape, dtype=np.float32)
     if w.needles:
-        q0 = query_walk_f32(w.with_(steps=1), layer)[0]          # [B][Hq][D]
-        qh = q0.reshape(w.batch, w.n_kv_heads, w.group, w.head_dim).sum(axis=2)
-        qh = qh / np.linalg.norm(qh, axis=-1, keepdims=True)
+        if qh is None:
+            qh = _needle_dirs(w, layer)
         P = w.page_size
-        for b, pages in enumerate(needle_pages(w)):
-            for p in pages:
-                k[b, p * P:(p + 1) * P] += np.float32(0.5) * qh[b][None, :, :]
+        for p in needle_pages(w)[b]:
+            k[p * P:(p + 1) * P] += np.float32(0.5) * qh[b][None, :, :]
     return k, v
 
 
@@ -204,15 +211,32 @@ def store_batch(w: Workload, layer: int):
     """Everything one prefill stores for one layer, flattened over requests:
     k_bits, v_bits [T][Hkv][D] (uint16) and logical token ids pos [T] (int64),
     request-major, strictly increasing."""
-    k, v = kv_f32(w, layer)
+    import concurrent.futures as cf
+    import os
     bt = block_table(w)
     P = w.page_size
-    ks, vs, ps = [], [], []
-    for b in range(w.batch):
-        n_tok = int(w.lens[b])
-        t = np.arange(n_tok, dtype=np.int64)
-        ps.append(bt[b][t // P].astype(np.int64) * P + t % P)
-        ks.append(k[b, :n_tok])
-        vs.append(v[b, :n_tok])
-    return (to_bf16_bits(np.concatenate(ks)), to_bf16_bits(np.concatenate(vs)),
-            np.concatenate(ps))
+    qh = _needle_dirs(w, layer)
+    lens = [int(x) for x in w.lens]
+    T = sum(lens)
+    HD = (w.n_kv_heads, w.head_dim)
+    kb = np.empty((T,) + HD, np.uint16)
+    vb = np.empty((T,) + HD, np.uint16)
+    pos = np.empty((T,), np.int64)
+    start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+
+    def one(b):
+        k, v = kv_request_f32(w, layer, b, qh)
+        t0, t1 = start[b], start[b + 1]
+        kb[t0:t1] = to_bf16_bits(k)
+        vb[t0:t1] = to_bf16_bits(v)
+        t = np.arange(lens[b], dtype=np.int64)
+        pos[t0:t1] = bt[b][t // P].astype(np.int64) * P + t % P
+
+    workers = max(1, min(w.batch, os.cpu_count() or 1))
+    if workers == 1:
+        for b in range(w.batch):
+            one(b)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(one, range(w.batch)))
+    return kb, vb, pos

@@ -6,6 +6,7 @@
 #include <climits>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 
@@ -73,16 +74,7 @@ int check_cache(const Dims& d, const ssa_cache* c) {
   return SSA_OK;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      n = 152;
-  }
-  return n;
-}
+int num_sms() { return current_device_info().sms; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -122,6 +114,37 @@ T* at(void* ws, size_t off) {
 }  // namespace
 
 void count_launch(int n) { g_launches += n; }
+
+// One entry per device ordinal, filled on first use with that device current.
+// A host may hold GPUs of different kinds, so nothing is shared between them.
+DeviceInfo current_device_info() {
+  static std::mutex mu;
+  static DeviceInfo info[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return DeviceInfo{152, 227 * 1024};
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& d = info[dev];
+  if (d.sms == 0) {
+    int sms = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms < 1)
+      sms = 152;
+    if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        smem < 48 * 1024)
+      smem = 48 * 1024;
+    d.smem_optin = smem;
+    d.sms = sms;
+  }
+  return d;
+}
+
+int current_device_ordinal() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return dev;
+}
 
 int validate_layout(const ssa_layout* lay, Dims& d) { return check_layout(lay, d); }
 

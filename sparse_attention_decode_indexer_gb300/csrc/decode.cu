@@ -48,6 +48,7 @@
 // the G-row tiles, the memory system sets the pace.
 #include <cudaTypedefs.h>
 #include <cuda.h>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -1010,13 +1011,17 @@ size_t decode_smem() {
 // that every CTA gets at least two tiles and no unit more than 130 pieces.
 template <bool FP8, int P>
 int decode_grid(const Dims& d, int n_layers, int num_sms) {
-  static int occ = -1;
-  if (occ < 0) {
+  // per device: the occupancy calculator's answer depends on the GPU
+  static std::atomic<int> occ_of[kMaxDevices];
+  std::atomic<int>& slot = occ_of[current_device_ordinal()];
+  int occ = slot.load(std::memory_order_relaxed);
+  if (occ < 1) {
     int o = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<FP8, P>, kDecodeThreads,
                                                       decode_smem<FP8, P>()) != cudaSuccess)
       o = 1;
     occ = o < 1 ? 1 : (o > Cfg<FP8, P>::kCtasPerSm ? Cfg<FP8, P>::kCtasPerSm : o);
+    slot.store(occ, std::memory_order_relaxed);
   }
   const int w = d.max_selected();
   const long long T = (long long)n_layers * d.B * d.Hkv * w;

@@ -73,6 +73,9 @@ constexpr int kSmemKeys = 16384;
 // Up to this many misses, the victim order is found by all-pairs ranking
 // (one pass, one barrier); beyond it by a bitonic sort.
 constexpr int kRankMax = 1024;
+// Upper bound on the ensure kernel's static shared memory (hist, scan
+// scratch, a few scalars), budgeted beside its dynamic buffers.
+constexpr size_t kEnsureStaticSmem = 2048;
 
 template <bool KEYS_IN_SMEM>
 __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsureParams p) {
@@ -418,8 +421,14 @@ cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, i
   p.has_mirror = c.k_mirror != nullptr;
   // small batches and pools: 256 threads (cheaper barriers); else 1024
   const int threads = (p.N2 <= 1024 && d.S <= 4096) ? 256 : kEnsureThreads;
-  const bool keys_in_smem = d.S <= kSmemKeys;
-  const size_t smem = (size_t)p.N2 * 12 + (keys_in_smem ? (size_t)d.S * 4 : 0);
+  // the slots' victim keys stay in shared memory when they fit beside the id
+  // and victim buffers (and the kernel's static shared memory) within the
+  // device's per-CTA limit; otherwise every radix pass reads them again
+  const size_t base = (size_t)p.N2 * 12;
+  const size_t with_keys = base + (size_t)d.S * 4;
+  const bool keys_in_smem =
+      d.S <= kSmemKeys && with_keys + kEnsureStaticSmem <= (size_t)current_device_info().smem_optin;
+  const size_t smem = keys_in_smem ? with_keys : base;
   auto k = keys_in_smem ? ensure_state_kernel<true> : ensure_state_kernel<false>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

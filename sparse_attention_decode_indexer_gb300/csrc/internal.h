@@ -73,6 +73,14 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+// Properties of the current device, queried once per device ordinal and
+// cached (SM count; the most dynamic shared memory one CTA may opt in to).
+constexpr int kMaxDevices = 64;
+struct DeviceInfo { int sms, smem_optin; };
+DeviceInfo current_device_info();
+// The current device's ordinal, clamped to [0, kMaxDevices).
+int current_device_ordinal();
+
 // Counts every kernel launch the library enqueues (per host thread).
 void count_launch(int n = 1);
 

@@ -127,6 +127,7 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
     bt = wl.block_table(w)
     max_err = 0.0
     misses = 0
+    max_layer_misses = 0
     for t in range(steps):
         q = np.stack([qs[l][t] for l in range(w.n_layers)])
         qd = _u16_to_bf16(q).cuda()
@@ -152,6 +153,7 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
             max_err = max(max_err, err)
             assert err <= TOL[w.fp8], f"max abs err {err} layer {l} step {t}"
             misses += nm
+            max_layer_misses = max(max_layer_misses, nm)
     if report is not None:
-        report.update(max_err=max_err, misses=misses)
+        report.update(max_err=max_err, misses=misses, max_layer_misses=max_layer_misses)
     return run, orc

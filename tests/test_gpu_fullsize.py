@@ -3,6 +3,12 @@ launch configuration: the library runs every layer in one launch per stage;
 the oracle (which finishes a layer in seconds) checks sampled layers after
 every decode step of the query walk.  Bit-exact selection, remap, miss lists
 and LRU state each step; pool bytes at the end; outputs within tolerance.
+
+The throughput sweep (131,072-token requests, 32/4 heads) runs at its full
+per-layer sizes for every batch, with one layer so that the oracle's copy of
+the host mirror fits the host: 64 and 32 requests over a 20 %-resident pool
+(26,215 and 13,108 slots per layer; 2,112 and 1,056 misses in the first step
+from the empty pool), and 8 requests fully resident, in bf16 and fp8.
 """
 import pytest
 
@@ -45,4 +51,20 @@ def test_sweep_128k_batch1_full(fp8, frac):
     w = wl.sweep_workload(1, fp8, frac, steps=6)
     rep = {}
     run_parity(w, oracle_layers=[3], pool_every_step=False, report=rep)
+    print(w.name, rep)
+
+
+SWEEP_FULL = [(64, True, 0.2), (64, False, 0.2), (32, True, 0.2), (32, False, 0.2),
+              (8, False, 1.0), (8, True, 1.0)]
+
+
+@pytest.mark.parametrize("batch,fp8,frac", SWEEP_FULL,
+                         ids=[f"b{b}_{'fp8' if f else 'bf16'}_{'resident' if r >= 1 else '20pct'}"
+                              for b, f, r in SWEEP_FULL])
+def test_sweep_128k_full_per_layer_sizes(batch, fp8, frac):
+    w = wl.sweep_workload(batch, fp8, frac, steps=3).with_(n_layers=1)
+    rep = {}
+    run_parity(w, pool_every_step=False, check_mirror=frac < 1.0, report=rep)
+    if frac < 1.0:
+        assert rep["max_layer_misses"] >= batch * (w.block_topk + 1)   # the cold first step
     print(w.name, rep)

@@ -5,8 +5,10 @@ scratch is a fixed array inside the library instead of a caller workspace.
 
 Called through the C ABI and compared with ssa_index_topk, which takes a
 workspace, on two calls in a row (the second reuses the array the first left
-behind).  Selection results are integers, so the comparison is exact.  The
-file runs last so that a failure here leaves every other test already run.
+behind), and with the oracle's selection directly (the call runs its own pair
+of kernels, a score kernel and a separate select kernel).  Selection results
+are integers, so the comparisons are exact.  The file runs last so that a
+failure here leaves every other test already run.
 """
 import ctypes
 
@@ -28,11 +30,13 @@ def _w():
 def test_static_scratch_matches_workspace_entry_point_on_two_calls():
     import torch
     import sparse_attention_decode_indexer_gb300 as ssa
-    from tests.parity import gpu_runner, prefill
+    from tests.parity import gpu_runner, oracle_state, prefill
 
     w = _w()
     run = gpu_runner(w)
-    prefill(w, run, None, oracle_layers=[])
+    orc = oracle_state(w)
+    prefill(w, run, orc, oracle_layers=list(range(w.n_layers)))
+    bt = wl.block_table(w)
     L = ssa.lib()
     fn = L.ssa_index_topk_static_scratch
     fn.restype = ctypes.c_int
@@ -58,6 +62,11 @@ def test_static_scratch_matches_workspace_entry_point_on_two_calls():
         assert torch.equal(sel_b, run.sel), f"call {t}"
         assert torch.equal(nsel_b, run.n_sel), f"call {t}"
         assert (run.n_sel == w.block_topk + 1).all()
+        for l in range(w.n_layers):
+            o_sel, o_nsel, _, drops, bad = orc.index_topk(l, q_all[t][l], bt, w.lens)
+            assert drops == 0 and bad == 0
+            assert np.array_equal(sel_b[l].cpu().numpy(), o_sel), f"call {t} layer {l}"
+            assert np.array_equal(nsel_b[l].cpu().numpy(), o_nsel), f"call {t} layer {l}"
 
 
 def test_static_scratch_rejects_calls_beyond_its_size():

@@ -91,8 +91,8 @@ def reduce_max(x: float, dist, device) -> float:
 
 
 # DRAM bytes (read + write) of one decode launch on lru_pressure_64k_fp8, from
-# the ncu capture summarised in profiles/decode_kernel_fp8_p64_lru_pressure_64k.md,
-# valid only for the kernel sources it was taken on (their SHA-256 below).
+# the committed ncu capture of the attention kernel on that workload, valid
+# only for the kernel sources it was taken on (their SHA-256 below).
 DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53115136 + 289792,
                   "sources": ("sparse_attention_decode_indexer_gb300/csrc/decode.cu",
                               "sparse_attention_decode_indexer_gb300/csrc/common.cuh"),
@@ -211,32 +211,71 @@ class ClockSampler:
 # the CPU oracle on a bounded sample (reported baseline; also --impl reference)
 # ---------------------------------------------------------------------------
 
-def cpu_oracle_sample(w: wl.Workload, seconds: float):
+def _oracle_state(w: wl.Workload):
+    """The oracle's state for layer 0 of the workload after its prefill."""
     import oracle
-    oracle.build()
     lay = oracle.OracleLayout(w.page_size, w.n_q_heads, w.n_kv_heads, w.head_dim, w.fp8,
-                              w.n_layers, w.logical_pages, w.slots, w.batch,
-                              w.pages_per_request, w.block_topk)
-    one = wl.Workload(**{**w.__dict__, "n_layers": 1})
-    lay.n_layers = 1
+                              1, w.logical_pages, w.slots, w.batch, w.pages_per_request,
+                              w.block_topk)
     orc = oracle.OracleKV(lay, host_tier=w.host_tier, identity=not w.host_tier)
-    k, v, pos = wl.store_batch(one, 0)
+    k, v, pos = wl.store_batch(w.with_(n_layers=1), 0)
     orc.store(0, k, v, pos)
+    return orc
+
+
+def _oracle_leg(w: wl.Workload, orc, seconds: float, threads: int, t_start: int):
+    """Decode steps of layer 0 (every request) through the oracle with the
+    given thread count, for about `seconds`; per-stage and total rates."""
+    import oracle
+    oracle.set_threads(threads)
+    one = w.with_(n_layers=1)
     qs = wl.queries(one.with_(steps=max(w.steps, 64)) if w.rho is not None else one, 0)
     bt = wl.block_table(w)
+    stage_s = {"index_topk": 0.0, "ensure": 0.0, "remap": 0.0, "decode": 0.0}
     steps = 0
     t0 = time.perf_counter()
     while True:
-        orc.step(0, qs[steps % len(qs)], bt, w.lens)
+        q = qs[(t_start + steps) % len(qs)]
+        ta = time.perf_counter()
+        sel, _, _, _, _ = orc.index_topk(0, q, bt, w.lens)
+        tb = time.perf_counter()
+        orc.ensure(0, sel, bt)
+        tc = time.perf_counter()
+        phys, _ = orc.remap(0, sel, bt)
+        td = time.perf_counter()
+        orc.decode(0, q, sel, phys, w.lens)
+        te = time.perf_counter()
+        for name, dt in (("index_topk", tb - ta), ("ensure", tc - tb), ("remap", td - tc),
+                         ("decode", te - td)):
+            stage_s[name] += dt
         steps += 1
-        if time.perf_counter() - t0 >= seconds:
+        if te - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    value = steps * w.batch / dt
-    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"layer 0 of {w.name}, all {w.batch} requests, {steps} decode steps "
-                      f"(index, select, ensure+copy, remap, fp64 attention), single thread, "
-                      f"{dt:.1f} s; prefill not timed"}
+    used = oracle.threads()
+    oracle.set_threads(0)
+    return {"value": steps * w.batch / dt, "steps": steps, "seconds": dt, "threads": used,
+            "stage_ms_per_step": {k: 1e3 * v / steps for k, v in stage_s.items()}}
+
+
+def cpu_oracle_sample(w: wl.Workload, seconds: float):
+    """The oracle as it stands, on the host cores, on a bounded sample (layer 0
+    of the workload, every request; the prefill is not timed): once on one
+    thread, once with its independent loops spread over every core (the
+    headline figure).  Per-stage times for both."""
+    import oracle
+    oracle.build()
+    orc = _oracle_state(w)
+    single = _oracle_leg(w, orc, seconds / 2, 1, 0)
+    multi = _oracle_leg(w, orc, seconds / 2, 0, single["steps"])
+    return {"value": multi["value"], "unit": UNIT, "cores": multi["threads"], "kind": "oracle",
+            "sample": f"layer 0 of {w.name}, all {w.batch} requests, {multi['steps']} decode "
+                      f"steps (index, select, ensure+copy, remap, fp64 attention) on "
+                      f"{multi['threads']} threads in {multi['seconds']:.1f} s; prefill not timed",
+            "stage_ms_per_step": multi["stage_ms_per_step"],
+            "single_thread": {"value": single["value"], "unit": UNIT, "cores": 1,
+                              "steps": single["steps"],
+                              "stage_ms_per_step": single["stage_ms_per_step"]}}
 
 
 # ---------------------------------------------------------------------------
@@ -256,15 +295,43 @@ def build_runner(w: wl.Workload, rank: int, prefill_now: bool = True):
     return run
 
 
+def draws_on_device(w: wl.Workload) -> bool:
+    """Inputs drawn on the device (torch's Philox generator) where drawing them
+    on the host would take minutes and tens of GB of host memory: more than
+    4 GiB of bf16 K+V per layer (the 32- and 64-request sweeps).  Same
+    distributions (N(0, 1) K, V; the same query walk), other random numbers."""
+    return int(w.lens.sum()) * w.n_kv_heads * w.head_dim * 4 > (4 << 30)
+
+
 def prefill(w: wl.Workload, run):
     """Store every layer's K/V of the workload through ssa_store_kv_mirror."""
     import torch
-    for l in range(w.n_layers):
-        k, v, pos = wl.store_batch(w, l)
-        kd = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).cuda()[None]
-        vd = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda()[None]
-        run.store(l, 1, kd, vd, torch.from_numpy(pos).cuda())
-        del kd, vd
+    if draws_on_device(w):
+        assert w.needles == 0
+        bt = torch.from_numpy(wl.block_table(w)).cuda()
+        P, HD = w.page_size, (w.n_kv_heads, w.head_dim)
+        per_req = int(w.lens.max())
+        chunk = max(1, (1 << 30) // (per_req * w.n_kv_heads * w.head_dim * 4))
+        for l in range(w.n_layers):
+            g = torch.Generator(device="cuda")
+            g.manual_seed(w.seed * 1000003 + l)
+            for b0 in range(0, w.batch, chunk):
+                bs = range(b0, min(w.batch, b0 + chunk))
+                pos = torch.cat([bt[b][torch.arange(int(w.lens[b]), device="cuda") // P] * P +
+                                 torch.arange(int(w.lens[b]), device="cuda") % P
+                                 for b in bs]).to(torch.int64)
+                T = int(pos.numel())
+                kd = torch.randn((1, T) + HD, generator=g, device="cuda").to(torch.bfloat16)
+                vd = torch.randn((1, T) + HD, generator=g, device="cuda").to(torch.bfloat16)
+                run.store(l, 1, kd, vd, pos)
+                del kd, vd, pos
+    else:
+        for l in range(w.n_layers):
+            k, v, pos = wl.store_batch(w, l)
+            kd = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).cuda()[None]
+            vd = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda()[None]
+            run.store(l, 1, kd, vd, torch.from_numpy(pos).cuda())
+            del kd, vd
     torch.cuda.synchronize()
     st = int(run.status.item())
     if st != 0:
@@ -272,9 +339,60 @@ def prefill(w: wl.Workload, run):
 
 
 def queries_all(w: wl.Workload, n_steps: int):
-    """[n_steps][L][B][Hq][D] bf16 bit patterns of the query walk."""
+    """[n_steps][L][B][Hq][D] bf16 queries of the walk, on the device."""
+    import torch
+    if draws_on_device(w):
+        shape = (w.batch, w.n_q_heads, w.head_dim)
+        out = torch.empty((n_steps, w.n_layers) + shape, dtype=torch.bfloat16, device="cuda")
+        for l in range(w.n_layers):
+            g = torch.Generator(device="cuda")
+            g.manual_seed(w.seed * 1000003 + 500 + l)
+            q = torch.randn(shape, generator=g, device="cuda")
+            out[0, l] = q.to(torch.bfloat16)
+            for t in range(1, n_steps):
+                q = w.rho * q + w.walk_c * torch.randn(shape, generator=g, device="cuda")
+                out[t, l] = q.to(torch.bfloat16)
+        return out
     ww = w.with_(steps=n_steps)
-    return np.stack([wl.queries(ww, l) for l in range(w.n_layers)], axis=1)
+    q_np = np.stack([wl.queries(ww, l) for l in range(w.n_layers)], axis=1)
+    return torch.from_numpy(q_np.view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host_link_rates(torch, ssa, page_chunk: int, scatter_chunks: int) -> dict:
+    """SM-driven reads of pinned host memory (ssa_host_read_probe), beside the
+    copy engine: a sequential stream of 64 KiB chunks over 1 GiB, and a
+    scatter of `scatter_chunks` page-sized chunks at random offsets (fresh
+    offsets each repetition), the access pattern of one step's miss fetch."""
+    n = 1 << 30
+    src = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    src.fill_(1)
+    dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+    out = {}
+
+    def timed(offsets, chunk, lpt):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        ssa.ssa_host_read_probe(src, dst, offsets, chunk, lpt)
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e-3
+
+    seq = torch.arange(0, n, 65536, dtype=torch.int64, device="cuda")
+    for lpt in (8, 16):
+        timed(seq, 65536, lpt)
+        best = min(timed(seq, 65536, lpt) for _ in range(4))
+        out[f"sm_read_seq_gbs_lpt{lpt}"] = n / best / 1e9
+    rng = np.random.default_rng(11)
+    n_pages = n // page_chunk
+    # every chunk lies inside the 1 GiB source, and the copies fit the 1 GiB dst
+    for cnt in sorted({max(1, min(scatter_chunks, n_pages, 65535)), min(4096, n_pages)}):
+        ts = []
+        for _ in range(5):
+            offs = rng.choice(n_pages, size=cnt, replace=False).astype(np.int64) * page_chunk
+            ts.append(timed(torch.from_numpy(offs).cuda(), page_chunk, 8))
+        out[f"sm_read_scatter_{cnt}x{page_chunk}B_gbs"] = cnt * page_chunk / statistics.median(ts) / 1e9
+    del src, dst
+    return out
 
 
 def h2d_peak_gbs(torch) -> float:
@@ -301,8 +419,7 @@ def run_ours(args, rank: int, world: int, dist):
     H_max = args.host_warmup if args.host_warmup >= 0 else (300 if w.host_tier else 0)
     run = build_runner(w, rank, prefill_now=False)   # graphs first, then one prefill
     n_total = H_max + W + 4 * K
-    q_np = queries_all(w, n_total)
-    q_all = torch.from_numpy(q_np.view(np.int16)).view(torch.bfloat16).cuda()
+    q_all = queries_all(w, n_total)
     q_cur = q_all[0].clone()
     flush_w = torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB > L2
     flush_r = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
@@ -490,8 +607,7 @@ def run_ours(args, rank: int, world: int, dist):
     # end to end through the public API, host buffers in and out
     e2e = None
     if not args.no_e2e:
-        q_host = torch.from_numpy(q_np[H + W + 3 * K:H + W + 4 * K].view(np.int16)).view(
-            torch.bfloat16).pin_memory()
+        q_host = q_all[H + W + 3 * K:H + W + 4 * K].cpu().pin_memory()
         out_host = torch.empty((K,) + tuple(run.out.shape), dtype=torch.bfloat16,
                                pin_memory=True)
         q_dev = torch.empty_like(q_cur)
@@ -525,6 +641,11 @@ def run_ours(args, rank: int, world: int, dist):
     miss_bytes = misses * page_fetch_bytes(w) / K
     stage_miss_bytes = int(stage_miss.sum().item()) * page_fetch_bytes(w) / K
     h2d = h2d_peak_gbs(torch)
+    esz = 1 if w.fp8 else 2
+    head_page = w.n_kv_heads * w.page_size * w.head_dim * esz     # one tensor of one page
+    link = host_link_rates(torch, ssa, head_page, max(1, int(round(2 * misses / K))))
+    uva_peak = max(v for k, v in link.items() if k.startswith("sm_read_seq"))
+    miss_gbs = stage_miss_bytes / (ens_ms * 1e-3) / 1e9
     # pages the step selects (every layer and request): those already bound
     # are the ones the pool kept from earlier steps, fetched by no one now
     sel_per_step = w.n_layers * int(n_selected(w).sum())
@@ -541,6 +662,9 @@ def run_ours(args, rank: int, world: int, dist):
                    "block_topk": w.block_topk, "pool_slots": w.slots,
                    "host_tier": w.host_tier, "layers_per_launch": w.n_layers,
                    "l2": "flushed between timed steps (256 MiB write + 256 MiB read)",
+                   "inputs": ("K/V and queries drawn on the device (torch Philox), N(0,1) "
+                              "rounded to bf16" if draws_on_device(w) else
+                              "K/V and queries from the seeded numpy generators (workloads)"),
                    "host_warmup_steps": H,
                    "timing": timing_mode},
         "roofline": {"kernel": "ssa_sparse_paged_decode (decode_kernel: attention and split merge)",
@@ -556,8 +680,10 @@ def run_ours(args, rank: int, world: int, dist):
                  "resident_fraction": 1.0 - (misses / K) / sel_per_step,
                  "gbs_over_ensure_stage": stage_miss_bytes / (ens_ms * 1e-3) / 1e9,
                  "h2d_copy_engine_peak_gbs": h2d,
-                 "frac_of_h2d_peak": (stage_miss_bytes / (ens_ms * 1e-3) / 1e9 / h2d
-                                      if h2d else None),
+                 "frac_of_h2d_peak": miss_gbs / h2d if h2d else None,
+                 "sm_read_peak_gbs": uva_peak,
+                 "frac_of_sm_read_peak": miss_gbs / uva_peak if uva_peak else None,
+                 "host_link": link,
                  "note": "the ensure stage is the LRU state kernel plus the copy kernel",
                  "warmup_ensure_us": ({"first": ens_us[0], "step_10": ens_us[min(9, len(ens_us) - 1)],
                                        "last_10_median": statistics.median(ens_us[-10:])}

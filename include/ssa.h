@@ -306,6 +306,23 @@ int ssa_index_topk_static_scratch(const ssa_layout *lay, const ssa_cache *c, int
  */
 int ssa_selftest_bounded_wait(int32_t *status, ssa_stream_t stream);
 
+/*
+ * Measurement helper (no counterpart in the pages): the host link's rate for
+ * reads issued by SMs, the access the miss fetch makes.  Copies n_chunks
+ * chunks of chunk_bytes each, chunk i starting at byte offsets[i] of src,
+ * into dst (chunk i at i * chunk_bytes), with 16-byte loads, loads_per_thread
+ * (4, 8 or 16) in flight per thread, one group of 256-thread CTAs per chunk.
+ *   src      pinned host memory the GPU can address (or device memory)
+ *   dst      device memory, n_chunks * chunk_bytes bytes
+ *   offsets  [n_chunks] int64, device memory; multiples of 16, and every
+ *            chunk must lie inside the caller's source buffer (not checked:
+ *            the values live on the device)
+ * chunk_bytes a multiple of 16; 1 <= n_chunks <= 65535; src and dst 16-byte
+ * aligned.  SSA_ERR_INVALID_ARG otherwise.  Time it with events on `stream`.
+ */
+int ssa_host_read_probe(const void *src, void *dst, const int64_t *offsets, int n_chunks,
+                        int chunk_bytes, int loads_per_thread, ssa_stream_t stream);
+
 /* Text for an SSA_ERR_* code or an SSA_ST_* bit set. */
 const char *ssa_status_str(int code);
 

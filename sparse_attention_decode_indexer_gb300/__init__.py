@@ -32,7 +32,7 @@ ST_DROP, ST_BAD_ID, ST_MISS_NO_MIRROR, ST_UNRESOLVED, ST_BAD_POS, ST_TIMEOUT = 1
 EXPORTS = ("ssa_workspace_size", "ssa_lru_init", "ssa_store_kv_mirror", "ssa_index_topk",
            "ssa_ensure_resident", "ssa_remap_block_table", "ssa_sparse_paged_decode",
            "ssa_status_str", "ssa_last_cuda_error", "ssa_launch_count",
-           "ssa_index_topk_static_scratch", "ssa_selftest_bounded_wait")
+           "ssa_index_topk_static_scratch", "ssa_selftest_bounded_wait", "ssa_host_read_probe")
 
 
 class SsaError(RuntimeError):
@@ -89,6 +89,8 @@ def lib():
         L.ssa_launch_count.argtypes = []
         L.ssa_selftest_bounded_wait.restype = i32
         L.ssa_selftest_bounded_wait.argtypes = [vp, vp]
+        L.ssa_host_read_probe.restype = i32
+        L.ssa_host_read_probe.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         _lib = L
     return _lib
 
@@ -255,6 +257,15 @@ def ssa_selftest_bounded_wait(status, stream=None):
     """One CTA waits on an mbarrier nothing arrives on; the bounded wait gives
     up after about a second and sets ST_TIMEOUT in ``status``."""
     _check(lib().ssa_selftest_bounded_wait(_ptr(status), _stream(stream)))
+
+
+def ssa_host_read_probe(src, dst, offsets, chunk_bytes: int, loads_per_thread: int = 8,
+                        stream=None):
+    """Copy chunks of ``src`` (pinned host or device) at the int64 byte
+    ``offsets`` (a device tensor) into ``dst`` with SM loads: the host link's
+    rate for the access pattern of the miss fetch."""
+    _check(lib().ssa_host_read_probe(_ptr(src), _ptr(dst), _ptr(offsets), int(offsets.numel()),
+                                     int(chunk_bytes), int(loads_per_thread), _stream(stream)))
 
 
 def launch_count() -> int:

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT = os.path.join(HERE, "libssa_gb300.so")
 OBJDIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "store.cu", "index.cu", "ensure.cu", "decode.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "store.cu", "index.cu", "ensure.cu", "decode.cu", "noalloc.cu", "selftest.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", INCLUDE]

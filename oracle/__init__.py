@@ -79,6 +79,8 @@ def _load():
         lib.or_remap.argtypes = [vp] * 5
         lib.or_decode.restype = None
         lib.or_decode.argtypes = [vp] * 9 + [ctypes.c_double, vp]
+        lib.or_prefetch.restype = i32
+        lib.or_prefetch.argtypes = [vp, i32] + [vp] * 18
         lib.or_set_threads.restype = None
         lib.or_set_threads.argtypes = [i32]
         lib.or_threads.restype = i32
@@ -225,6 +227,28 @@ class OracleKV:
             _p(self._mir(self.v_mirror, l)), _p(self._mir(self.k_scale_m, l)),
             _p(self._mir(self.v_scale_m, l)), _p(self.k_pool[l]), _p(self.v_pool[l]),
             _p(self.k_scale[l]), _p(self.v_scale[l]), _p(mp), _p(ms), _p(nm))
+        return mp, ms, int(nm[0]), flags
+
+    # -- NEXT-1: top-k preload ----------------------------------------------
+    def prefetch(self, layer: int, width: int, scores: np.ndarray, seq_lens: np.ndarray,
+                 bt: np.ndarray):
+        """Fetch ahead the top (width-1) pages + last page of each request by a
+        step's scores, after that step's ensure (or_prefetch)."""
+        lib, lay = _load(), self.lay.c()
+        BW = self.lay.batch * self.lay.max_sel
+        l = layer
+        mp = np.empty((BW,), np.int32)
+        ms = np.empty((BW,), np.int32)
+        nm = np.zeros((1,), np.int32)
+        flags = lib.or_prefetch(
+            ctypes.byref(lay), int(width), _p(self.slot_of[l]), _p(self.page_of[l]),
+            _p(self.last_use[l]), _p(self.clock[l:l + 1]),
+            _p(np.ascontiguousarray(scores, np.int32)),
+            _p(np.ascontiguousarray(seq_lens, np.int32)), _p(np.ascontiguousarray(bt, np.int32)),
+            _p(self._mir(self.k_mirror, l)), _p(self._mir(self.v_mirror, l)),
+            _p(self._mir(self.k_scale_m, l)), _p(self._mir(self.v_scale_m, l)),
+            _p(self.k_pool[l]), _p(self.v_pool[l]), _p(self.k_scale[l]), _p(self.v_scale[l]),
+            _p(mp), _p(ms), _p(nm))
         return mp, ms, int(nm[0]), flags
 
     # -- a5 ------------------------------------------------------------------

@@ -473,6 +473,118 @@ int or_ensure(const or_layout *L, int32_t *slot_of, int32_t *page_of,
 }
 
 /* ------------------------------------------------------------------------ */
+/* NEXT-1: top-k preload                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [RFC] "Motivation" point 2 and "Proposed Change / Topk KV preload": the
+ * top-k of adjacent decode steps overlap strongly, so a former top-k index can
+ * drive a fetch that runs while the current step computes, and only the pages
+ * still missing once the actual top-k is known are loaded synchronously.
+ *
+ * Reading (the pages give no rule; this one keeps the fixed shapes and the
+ * LRU above):
+ *   * it runs after a step's ensure, on that step's scores; e = clock - 1 is
+ *     the epoch of that ensure (its pages have last_use == e);
+ *   * candidates, per request: the top (width - 1) pages of [0, n-1) by
+ *     (score desc, page id asc) plus page n-1, all pages when n-1 <= width-1
+ *     (the selection of or_select with k = width - 1), width <= W;
+ *   * U = the distinct logical ids of the batch's candidates, ascending;
+ *   * resident ids of U are touched: last_use = e, as the step's own pages
+ *     are, so that the preload never evicts a candidate;
+ *   * the ids of U that are not resident, ascending, take victims in order:
+ *     free slots by ascending slot id, then bound slots with last_use < e by
+ *     ascending (last_use, slot) -- the pages the current step reads and
+ *     the candidates are never evicted; ids left over when the victims run
+ *     out are not fetched;
+ *   * each bound id gets last_use = e, its slot the mirror's bytes;
+ *   * the clock does not move, so the next ensure sees the preloaded pages
+ *     as resident (hits) and, among the slots its own step does not touch,
+ *     evicts the least recently used first.
+ */
+int or_prefetch(const or_layout *L, int width, int32_t *slot_of, int32_t *page_of,
+                int32_t *last_use, const int32_t *clock, const int32_t *scores,
+                const int32_t *seq_lens, const int32_t *bt,
+                const uint8_t *k_mirror, const uint8_t *v_mirror,
+                const float *k_scale_m, const float *v_scale_m,
+                uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float *v_scale,
+                int32_t *miss_page, int32_t *miss_slot, int32_t *n_miss) {
+  int flags = 0;
+  const int BW = L->B * L->W;
+  const int32_t e = *clock - 1;
+  if (width < 1 || width > L->W) return -1;
+  or_layout Lw = *L;
+  Lw.k = width - 1;
+  Lw.W = width;
+  int32_t *cand = (int32_t *)malloc(sizeof(int32_t) * (size_t)L->B * width);
+  int32_t *ncand = (int32_t *)malloc(sizeof(int32_t) * L->B);
+  or_select(&Lw, scores, seq_lens, cand, ncand);
+
+  int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * ((size_t)L->B * width + 1));
+  int nid = 0;
+  for (int b = 0; b < L->B; ++b)
+    for (int i = 0; i < ncand[b]; ++i) {
+      int p = cand[(size_t)b * width + i];
+      int id = bt[(size_t)b * L->n_max + p];
+      if (id < 0 || id >= L->Lp) { flags |= 2; continue; }
+      ids[nid++] = id;
+    }
+  qsort(ids, (size_t)nid, sizeof(int32_t), int_cmp);
+  int nu = 0;
+  for (int i = 0; i < nid; ++i)
+    if (nu == 0 || ids[nu - 1] != ids[i]) ids[nu++] = ids[i];
+
+  /* touch the resident candidates */
+  for (int i = 0; i < nu; ++i)
+    if (slot_of[ids[i]] >= 0) last_use[slot_of[ids[i]]] = e;
+
+  /* victim order: free slots, then bound slots older than epoch e */
+  victim *cands = (victim *)malloc(sizeof(victim) * (L->S + 1));
+  int nc = 0;
+  for (int s = 0; s < L->S; ++s) {
+    if (page_of[s] >= 0 && last_use[s] >= e) continue;
+    cands[nc].key = page_of[s] < 0 ? -2 : last_use[s];
+    cands[nc].slot = s;
+    ++nc;
+  }
+  qsort(cands, (size_t)nc, sizeof(victim), victim_cmp);
+
+  const size_t esz = L->fp8 ? 1 : 2;
+  const size_t pbytes = page_elems(L) * esz;
+  int m = 0;
+  for (int i = 0; i < nu && m < nc; ++i) {
+    int id = ids[i];
+    if (slot_of[id] >= 0) continue;
+    int v = cands[m].slot;
+    int old = page_of[v];
+    if (old >= 0) slot_of[old] = -1;
+    slot_of[id] = v;
+    page_of[v] = id;
+    last_use[v] = e;
+    if (k_mirror && v_mirror) {
+      memcpy(k_pool + (size_t)v * pbytes, k_mirror + (size_t)id * pbytes, pbytes);
+      memcpy(v_pool + (size_t)v * pbytes, v_mirror + (size_t)id * pbytes, pbytes);
+      if (L->fp8) {
+        memcpy(k_scale + (size_t)v * L->P, k_scale_m + (size_t)id * L->P, sizeof(float) * L->P);
+        memcpy(v_scale + (size_t)v * L->P, v_scale_m + (size_t)id * L->P, sizeof(float) * L->P);
+      }
+    } else {
+      flags |= 4;
+    }
+    miss_page[m] = id;
+    miss_slot[m] = v;
+    ++m;
+  }
+  for (int i = m; i < BW; ++i) miss_page[i] = miss_slot[i] = -1;
+  *n_miss = m;
+  free(cands);
+  free(ids);
+  free(ncand);
+  free(cand);
+  return flags;
+}
+
+/* ------------------------------------------------------------------------ */
 /* a5: remap                                                                 */
 /* ------------------------------------------------------------------------ */
 

@@ -418,7 +418,7 @@ def run_ours(args, rank: int, world: int, dist):
     W, K = args.warmup, args.steps
     H_max = args.host_warmup if args.host_warmup >= 0 else (300 if w.host_tier else 0)
     run = build_runner(w, rank, prefill_now=False)   # graphs first, then one prefill
-    n_total = H_max + W + 4 * K
+    n_total = H_max + W + 4 * K + (6 * K + 16 if w.host_tier else 0)
     q_all = queries_all(w, n_total)
     q_cur = q_all[0].clone()
     flush_w = torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB > L2
@@ -439,18 +439,15 @@ def run_ours(args, rank: int, world: int, dist):
                            None, run.status, run.ws)
 
     def st_ensure():
-        ssa.ssa_ensure_resident(c, 0, L, run.sel, run.block_table, run.miss_page, run.miss_slot,
-                                run.n_miss, run.status, run.ws)
-
-    def st_remap():
-        ssa.ssa_remap_block_table(c, 0, L, run.sel, run.block_table, run.phys, run.status)
+        # ensure (LRU state + miss copy) with the remap fused into the LRU kernel
+        ssa.ssa_ensure_remap(c, 0, L, run.sel, run.block_table, run.phys, run.miss_page,
+                             run.miss_slot, run.n_miss, run.status, run.ws)
 
     def st_decode():
         ssa.ssa_sparse_paged_decode(c, 0, L, q_cur, run.sel, run.phys, run.seq_lens,
                                     run.sm_scale, run.out, run.status, run.ws)
 
-    stages = [("index_topk", st_index), ("ensure", st_ensure), ("remap", st_remap),
-              ("decode", st_decode)]
+    stages = [("index_topk", st_index), ("ensure_remap", st_ensure), ("decode", st_decode)]
     # one eager step (function attributes, lazy init), then capture the step:
     # one graph with timing events between its stages (events recorded from
     # inside the graph), or, where this torch cannot record events in a
@@ -544,7 +541,7 @@ def run_ours(args, rank: int, world: int, dist):
     while H < H_max:
         flush_l2()                         # the same conditions as the timed steps
         q_cur.copy_(q_all[H])
-        ens_us.append(replay_step(warm_ev)[1] * 1e3)
+        ens_us.append(replay_step(warm_ev)[1] * 1e3)   # the ensure_remap stage
         H += 1
         if H >= 50:
             last, prev = statistics.median(ens_us[-10:]), statistics.median(ens_us[-20:-10])
@@ -629,6 +626,10 @@ def run_ours(args, rank: int, world: int, dist):
                "ms_per_step": 1e3 * tot / K,
                "path": "DecodeRunner.step (4 C-ABI calls, direct launches) + pinned H2D q / D2H out"}
 
+    preload = host_tail = None
+    if w.host_tier:
+        preload = time_preload(w, run, q_all, H + W + 4 * K, K, flush_l2)
+        host_tail = time_host_tail(w, run, q_all, H + W + 8 * K + 8, K, flush_l2)
     if rank != 0:
         return None
     store = time_store(w, run)
@@ -637,7 +638,7 @@ def run_ours(args, rank: int, world: int, dist):
     dec_bytes = decode_bytes(w)
     achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
     idx_ms = statistics.mean(stage_ms["index_topk"])
-    ens_ms = statistics.mean(stage_ms["ensure"])
+    ens_ms = statistics.mean(stage_ms["ensure_remap"])
     miss_bytes = misses * page_fetch_bytes(w) / K
     stage_miss_bytes = int(stage_miss.sum().item()) * page_fetch_bytes(w) / K
     h2d = h2d_peak_gbs(torch)
@@ -684,7 +685,7 @@ def run_ours(args, rank: int, world: int, dist):
                  "sm_read_peak_gbs": uva_peak,
                  "frac_of_sm_read_peak": miss_gbs / uva_peak if uva_peak else None,
                  "host_link": link,
-                 "note": "the ensure stage is the LRU state kernel plus the copy kernel",
+                 "note": "the ensure_remap stage is the LRU state kernel (remap fused) plus the copy kernel",
                  "warmup_ensure_us": ({"first": ens_us[0], "step_10": ens_us[min(9, len(ens_us) - 1)],
                                        "last_10_median": statistics.median(ens_us[-10:])}
                                       if ens_us else None)},
@@ -697,7 +698,122 @@ def run_ours(args, rank: int, world: int, dist):
     if e2e is not None:
         line["e2e"] = e2e
     line["store"] = store
+    if preload is not None:
+        line["preload"] = preload
+    if host_tail is not None:
+        line["host_tail"] = host_tail
     return line, w
+
+
+def time_preload(w: wl.Workload, run, q_all, t0: int, K: int, flush_l2):
+    """The top-k preload against plain steps, both through DecodeRunner.step
+    (eager launches, the preload on a second stream).  Two timings per
+    variant: (a) one step per timed region, L2 flushed before it, the region
+    closed only once the step's preload is done too, so the preload overlaps
+    the step's attention and nothing else; (b) K steps back to back in one
+    region, where the preload also overlaps the next step's indexer."""
+    import torch
+    width = 2 * w.block_topk + 8          # the widest preload the buffers take
+    main = torch.cuda.current_stream()
+    out = {"width": width}
+    t = t0
+    for name, wdt in (("plain", 0), ("preload", width)):
+        run.enable_preload(wdt)
+        for _ in range(3):                 # warm the variant
+            run.step(q_all[t]); t += 1
+        torch.cuda.synchronize()
+        ms, miss, fetched = [], 0, 0
+        for _ in range(K):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run.step(q_all[t]); t += 1
+            if wdt:
+                main.wait_stream(run.side)
+            e1.record()
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+            miss += int(run.n_miss.sum().item())
+            fetched += int(run.n_fetch.sum().item()) if wdt else 0
+        flush_l2()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            run.step(q_all[t]); t += 1
+        if wdt:
+            main.wait_stream(run.side)
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = {"ms_per_step": statistics.mean(ms),
+                     "value": w.n_layers * w.batch / (statistics.mean(ms) * 1e-3),
+                     "back_to_back_ms_per_step": e0.elapsed_time(e1) / K,
+                     "sync_misses_per_step": miss / K,
+                     "preloaded_pages_per_step": fetched / K}
+    run.enable_preload(0)
+    p, b = out["preload"], out["plain"]
+    out["sync_miss_fraction_hidden"] = (1.0 - p["sync_misses_per_step"] / b["sync_misses_per_step"]
+                                        if b["sync_misses_per_step"] else None)
+    out["step_time_ratio"] = p["ms_per_step"] / b["ms_per_step"]
+    out["back_to_back_ratio"] = p["back_to_back_ms_per_step"] / b["back_to_back_ms_per_step"]
+    out["note"] = ("eager DecodeRunner.step with and without ssa_prefetch_pages on a second "
+                   "stream; (a) per-step regions after an L2 flush, closed after the preload; "
+                   "(b) K steps back to back")
+    return out
+
+
+def time_host_tail(w: wl.Workload, run, q_all, t0: int, K: int, flush_l2):
+    """Zero-copy host-tail attention against ensure-then-attend, both eager,
+    one step per timed region after an L2 flush.  The zero-copy step is the
+    indexer plus ssa_sparse_paged_decode_host_tail: pages without a slot are
+    read from the host mirror inside the attention, the pool stays as the LRU
+    left it (a frozen HBM head).  Host pages per step are counted from sel and
+    slot_of after each step."""
+    import torch
+    import sparse_attention_decode_indexer_gb300 as ssa
+    L, c = w.n_layers, run.cache
+    t = t0
+
+    def zero_copy(q):
+        ssa.ssa_index_topk(c, 0, L, q, run.block_table, run.seq_lens, run.sel, run.n_sel, None,
+                           run.status, run.ws)
+        ssa.ssa_sparse_paged_decode_host_tail(c, 0, L, q, run.sel, run.block_table,
+                                              run.seq_lens, run.sm_scale, run.out, run.status,
+                                              run.ws)
+
+    out = {}
+    for name, fn in (("ensure_then_attend", lambda q: run.step(q)), ("zero_copy", zero_copy)):
+        for _ in range(3):
+            fn(q_all[t]); t += 1
+        torch.cuda.synchronize()
+        ms, host = [], 0
+        for _ in range(K):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn(q_all[t]); t += 1
+            e1.record()
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+            sel = run.sel.long()
+            bt = run.block_table.long()
+            ids = torch.gather(bt.unsqueeze(0).expand(L, -1, -1), 2, sel.clamp(min=0))
+            slot = torch.gather(c.slot_of.long(), 1, ids.reshape(L, -1)).reshape(ids.shape)
+            host += int(((sel >= 0) & (slot < 0)).sum().item())
+        out[name] = {"ms_per_step": statistics.mean(ms),
+                     "value": L * w.batch / (statistics.mean(ms) * 1e-3),
+                     "host_pages_per_step": host / K}
+    # a host page is one (layer, request) page: K and V of every KV head (+ scales)
+    out["zero_copy"]["host_bytes_per_step"] = (out["zero_copy"]["host_pages_per_step"] *
+                                               page_fetch_bytes(w))
+    out["ratio"] = out["zero_copy"]["ms_per_step"] / out["ensure_then_attend"]["ms_per_step"]
+    out["note"] = ("eager steps, L2 flushed before each; zero_copy = indexer + host-tail "
+                   "attention over the pool as the LRU left it (not updated), "
+                   "ensure_then_attend = DecodeRunner.step")
+    st = int(run.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the host-tail leg")
+    return out
 
 
 def time_store(w: wl.Workload, run, chunk: int = 4096, n_append: int = 50):

@@ -81,7 +81,9 @@ enum {
   SSA_ST_MISS_NO_MIRROR = 4,  /* a miss had no host mirror to fetch from     */
   SSA_ST_UNRESOLVED = 8,      /* a selected page had no slot at remap/decode */
   SSA_ST_BAD_POS = 16,        /* store positions not strictly increasing     */
-  SSA_ST_TIMEOUT = 32         /* a bounded device wait gave up               */
+  SSA_ST_TIMEOUT = 32,        /* a bounded device wait gave up               */
+  SSA_ST_INTERNAL = 64        /* a kernel's own consistency check failed (its
+                                 work was abandoned; report it as a bug)       */
 };
 
 enum { SSA_KV_BF16 = 0, SSA_KV_FP8_E4M3 = 1 };
@@ -153,7 +155,7 @@ size_t ssa_workspace_size(const ssa_layout *lay);
 
 /*
  * Reset the residency state of every layer (FreeToken PR #499, "What": the
- * GPU pool is an LRU cache of physical slots over the logical page space).
+ * GPU's slots cache logical pages, least recently used out first).
  *   identity = 0: empty pool (slot_of = page_of = last_use = -1, clock 0);
  *   identity = 1: fully resident, slot s holds logical page s for
  *                 s < min(S, Lp), last_use -1, clock 0.
@@ -164,9 +166,9 @@ int ssa_lru_init(const ssa_layout *lay, const ssa_cache *c, int identity,
 
 /*
  * a0 -- store K/V through the write-through mirror (FreeToken PR #499,
- * "Design": every store is mirrored to a pinned host bank, so GPU slots are
- * drop-clean; FreeToken PR #525: for fp8 the mirror receives the codes and
- * scales after quantisation).
+ * "Design": each stored token also goes to pinned host memory, so evicting a
+ * slot never needs a write-back; FreeToken PR #525: with fp8 the host copy
+ * holds the quantised codes and their scales, byte for byte the pool's).
  *   k, v   [n_layers][T][Hkv][D] bf16, device
  *   pos    [T] int64 logical token ids, page = pos / P, row j = pos % P;
  *          strictly increasing within the call (SSA_ST_BAD_POS otherwise),
@@ -214,10 +216,11 @@ int ssa_index_topk(const ssa_layout *lay, const ssa_cache *c, int layer0, int n_
                    void *ws, ssa_stream_t stream);
 
 /*
- * a3 + a4 -- LRU ensure and miss fetch (FreeToken PR #499, "Design": a
- * device-side LRU with fixed shapes, graph-safe; eviction is a pure rebind;
- * misses are copied host -> device; FreeToken PR #525: the copy carries the
- * scale banks, and the batch selection fits the pool by construction).
+ * a3 + a4 -- LRU ensure and miss fetch (FreeToken PR #499, "Design": the
+ * LRU runs on the device with fixed shapes, so it can sit in a CUDA graph;
+ * evicting only rebinds a slot; misses are copied host -> device; FreeToken
+ * PR #525: the copy includes the fp8 scales, and the pool is sized so that
+ * the whole batch's selection fits).
  * Per layer, in this order:
  *   1. U = distinct logical ids bt[b][sel[b][i]] of the batch, ascending;
  *   2. hits are touched: last_use[slot] = clock;
@@ -236,6 +239,57 @@ int ssa_ensure_resident(const ssa_layout *lay, const ssa_cache *c, int layer0, i
                         const int32_t *sel, const int32_t *block_table,
                         int32_t *miss_page_opt, int32_t *miss_slot_opt, int32_t *n_miss_opt,
                         int32_t *status, void *ws, ssa_stream_t stream);
+
+/*
+ * a3 + a4 + a5 in one call: ssa_ensure_resident, whose LRU kernel also
+ * writes the remapped table once every selected page has its slot -- the
+ * same phys as ssa_remap_block_table (FreeToken PR #499, "Design": after
+ * ensure the block table is translated logical -> physical), one launch
+ * fewer per step.
+ *   phys [n_layers][B][W] int32 out (required)
+ */
+int ssa_ensure_remap(const ssa_layout *lay, const ssa_cache *c, int layer0, int n_layers,
+                     const int32_t *sel, const int32_t *block_table, int32_t *phys,
+                     int32_t *miss_page_opt, int32_t *miss_slot_opt, int32_t *n_miss_opt,
+                     int32_t *status, void *ws, ssa_stream_t stream);
+
+/*
+ * Top-k preload (vLLM RFC #33980, "Motivation" point 2 and "Proposed Change":
+ * "Topk KV preload" -- adjacent decode steps select largely the same pages,
+ * so a former top-k can drive a fetch that overlaps the current step's
+ * compute, leaving only the residual misses to load once the actual top-k
+ * is known).  Run after a step's ssa_ensure_resident, on that step's scores:
+ *   1. candidates, per request: the top (width - 1) pages of [0, n_b - 1) by
+ *      (score desc, page asc) plus page n_b - 1 (all pages when
+ *      n_b - 1 <= width - 1) -- the selection rule with k = width - 1;
+ *   2. per layer, U = the distinct logical ids of the batch's candidates;
+ *      with e = clock - 1 (the epoch of the step's ensure):
+ *   3. resident ids of U are touched: last_use = e;
+ *   4. the other ids of U, ascending, take victims in order: free slots by
+ *      ascending slot id, then bound slots with last_use < e by ascending
+ *      (last_use, slot) -- so the pages the step's attention reads are never
+ *      evicted; ids left over when no victim remains are not fetched;
+ *   5. each bound id gets last_use = e and its K, V (and fp8 scales) are
+ *      copied mirror -> slot; the clock is not advanced.
+ * The next ssa_ensure_resident then finds the fetched pages resident.
+ *   scores        [n_layers][B][n_max] int32: the step's scores_opt from
+ *                 ssa_index_topk; must not change until this call completes
+ *   width         candidates per request, 1 <= width <= max_sel
+ *   fetch_page_opt, fetch_slot_opt  [n_layers][B*W] int32 out or NULL
+ *   n_fetch_opt   [n_layers] int32 out or NULL: pages fetched per layer
+ * ws is required (the candidates and fetch lists live in a part of it that
+ * no other call uses).  Ordering: after the step's ssa_remap_block_table
+ * (which reads the state this call changes) and before the next step's
+ * ssa_ensure_resident; it may run on a second stream concurrently with the
+ * step's ssa_sparse_paged_decode (the slots it reads are never victims) and
+ * the next step's ssa_index_topk (which must write its scores elsewhere).
+ * SSA_ERR_POOL_TOO_SMALL as ssa_ensure_resident.
+ */
+int ssa_prefetch_pages(const ssa_layout *lay, const ssa_cache *c, int layer0, int n_layers,
+                       const int32_t *scores, const int32_t *block_table,
+                       const int32_t *seq_lens, int width, int32_t *fetch_page_opt,
+                       int32_t *fetch_slot_opt, int32_t *n_fetch_opt, int32_t *status, void *ws,
+                       ssa_stream_t stream);
 
 /*
  * a5 -- block-table translation (FreeToken PR #499, "Design": after ensure
@@ -271,6 +325,28 @@ int ssa_sparse_paged_decode(const ssa_layout *lay, const ssa_cache *c, int layer
                             const void *q, const int32_t *sel, const int32_t *phys,
                             const int32_t *seq_lens, float sm_scale, void *out,
                             int32_t *status, void *ws, ssa_stream_t stream);
+
+/*
+ * Zero-copy host-tail attention (vLLM RFC #33980, the comment that maps one
+ * address range with an HBM-backed head and a host-backed tail, so that the
+ * attention reads the tail's slots over the interconnect with no staging
+ * copy).  The same attention as ssa_sparse_paged_decode, on sel and the
+ * block table instead of a remapped table: each selected page is resolved
+ * through slot_of; a resident page is read from its pool slot, a page with
+ * no slot straight from the pinned host mirror (16-byte loads over UVA into
+ * the same on-chip layout).  The residency state is not changed -- no
+ * ensure, no copy, no eviction -- so each step re-reads its host pages.
+ *   sel          [n_layers][B][W] from ssa_index_topk
+ *   block_table  [B][n_max] logical ids
+ * Requires the host mirror (SSA_ERR_NO_MIRROR); ws as for
+ * ssa_sparse_paged_decode.  Mirror bytes equal pool bytes, so the result is
+ * that of ensure + remap + ssa_sparse_paged_decode on the same selection.
+ */
+int ssa_sparse_paged_decode_host_tail(const ssa_layout *lay, const ssa_cache *c, int layer0,
+                                      int n_layers, const void *q, const int32_t *sel,
+                                      const int32_t *block_table, const int32_t *seq_lens,
+                                      float sm_scale, void *out, int32_t *status, void *ws,
+                                      ssa_stream_t stream);
 
 /*
  * ssa_index_topk without a workspace: the same indexer and top-k selection

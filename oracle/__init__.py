@@ -276,6 +276,27 @@ class OracleKV:
                       _p(np.ascontiguousarray(seq_lens, np.int32)), float(sm_scale), _p(out))
         return out
 
+    def decode_from_mirror(self, layer: int, q_bits: np.ndarray, sel: np.ndarray,
+                           bt: np.ndarray, seq_lens: np.ndarray, sm_scale: float | None = None):
+        """The attention over the selected pages read from the host mirror
+        (which holds the pool's bytes for every page): or_decode with the
+        mirror as the page store and the logical ids as its slots."""
+        lib, lay = _load(), self.lay.c()
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.lay.head_dim)
+        sel = np.ascontiguousarray(sel, np.int32)
+        ids = np.full_like(sel, -1)
+        for b in range(sel.shape[0]):
+            v = sel[b] >= 0
+            ids[b][v] = np.asarray(bt, np.int32)[b][sel[b][v]]
+        out = np.empty((self.lay.batch, self.lay.n_q_heads, self.lay.head_dim), np.float64)
+        l = layer
+        lib.or_decode(ctypes.byref(lay), _p(self.k_mirror[l]), _p(self.v_mirror[l]),
+                      _p(self.k_scale_m[l]), _p(self.v_scale_m[l]),
+                      _p(np.ascontiguousarray(q_bits, np.uint16)), _p(sel), _p(ids),
+                      _p(np.ascontiguousarray(seq_lens, np.int32)), float(sm_scale), _p(out))
+        return out
+
     # -- one whole decode step for one layer --------------------------------
     def step(self, layer: int, q_bits, bt, seq_lens, sm_scale=None) -> dict:
         sel, n_sel, scores, drops, bad = self.index_topk(layer, q_bits, bt, seq_lens)

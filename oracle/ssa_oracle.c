@@ -101,10 +101,10 @@ static size_t in_page(const or_layout *L, int h, int j, int d) {
 }
 
 /*
- * [FT499] "Design": every store_kv is mirrored to a pinned host bank, so a GPU
- * slot is always drop-clean.  [FT525]: for an fp8 pool the mirror holds the
- * e4m3 codes and fp32 scales taken AFTER quantisation (the pool is the source
- * of truth), so mirror and pool bytes are identical.
+ * [FT499] "Design": each stored token also goes to pinned host memory, so a
+ * slot can be evicted without a write-back.  [FT525]: with fp8 that host copy
+ * gets the quantised codes and their scales, so mirror and pool hold the same
+ * bytes.
  *
  * fp8 reading (per-token scale, [FT525] "the fp8 pool's per-token
  * _scale_buffer"): one fp32 scale per token per tensor over all KV heads,
@@ -379,12 +379,12 @@ static int victim_cmp(const void *a, const void *b) {
 }
 
 /*
- * [FT499] "What": the GPU pool is an LRU cache of physical slots over the
- * logical page space; "Design": lru_ensure is a device-side LRU with fixed
- * shapes, and eviction is a pure rebind (slots are drop-clean, no write-back);
- * misses are copied from the pinned mirror (fast_index_copy); [FT525]: the
- * copy carries the scale banks too, and the whole batch selection fits the
- * pool by construction.
+ * [FT499] "What" and "Design": the GPU's slots cache logical pages, the
+ * least recently used slot is reused first, the update has fixed shapes, and
+ * evicting only rebinds a slot (the host copy is always current, so nothing
+ * is written back); misses are copied from the pinned host copy; [FT525]: the
+ * copy includes the fp8 scales, and the pool is sized so that the batch's
+ * whole selection fits.
  *
  * Reading of the order of events (the pages state none):
  *   1. U = the distinct logical ids selected by the batch, ascending.

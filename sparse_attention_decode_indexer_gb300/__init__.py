@@ -11,6 +11,7 @@ library is missing or no GPU is present the calls raise.
     ssa_ensure_resident      device LRU + miss fetch from the host mirror
     ssa_remap_block_table    logical -> physical block table
     ssa_sparse_paged_decode  attention over the selected pages
+    ssa_prefetch_pages       top-k preload of the next step's likely pages
 """
 from __future__ import annotations
 
@@ -28,11 +29,13 @@ SSA_KV_BF16 = 0
 SSA_KV_FP8_E4M3 = 1
 
 ST_DROP, ST_BAD_ID, ST_MISS_NO_MIRROR, ST_UNRESOLVED, ST_BAD_POS, ST_TIMEOUT = 1, 2, 4, 8, 16, 32
+ST_INTERNAL = 64
 
 EXPORTS = ("ssa_workspace_size", "ssa_lru_init", "ssa_store_kv_mirror", "ssa_index_topk",
            "ssa_ensure_resident", "ssa_remap_block_table", "ssa_sparse_paged_decode",
            "ssa_status_str", "ssa_last_cuda_error", "ssa_launch_count",
-           "ssa_index_topk_static_scratch", "ssa_selftest_bounded_wait", "ssa_host_read_probe")
+           "ssa_index_topk_static_scratch", "ssa_selftest_bounded_wait", "ssa_host_read_probe",
+           "ssa_prefetch_pages", "ssa_ensure_remap", "ssa_sparse_paged_decode_host_tail")
 
 
 class SsaError(RuntimeError):
@@ -89,6 +92,15 @@ def lib():
         L.ssa_launch_count.argtypes = []
         L.ssa_selftest_bounded_wait.restype = i32
         L.ssa_selftest_bounded_wait.argtypes = [vp, vp]
+        L.ssa_sparse_paged_decode_host_tail.restype = i32
+        L.ssa_sparse_paged_decode_host_tail.argtypes = ([P(SsaLayout), P(SsaCache), i32, i32, vp,
+                                                         vp, vp, vp, ctypes.c_float, vp, vp, vp,
+                                                         vp])
+        L.ssa_ensure_remap.restype = i32
+        L.ssa_ensure_remap.argtypes = [P(SsaLayout), P(SsaCache), i32, i32] + [vp] * 9
+        L.ssa_prefetch_pages.restype = i32
+        L.ssa_prefetch_pages.argtypes = ([P(SsaLayout), P(SsaCache), i32, i32, vp, vp, vp, i32]
+                                         + [vp] * 6)
         L.ssa_host_read_probe.restype = i32
         L.ssa_host_read_probe.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         _lib = L
@@ -238,6 +250,26 @@ def ssa_ensure_resident(cache: KVCache, layer0: int, n_layers: int, sel, block_t
                                      _stream(stream)))
 
 
+def ssa_ensure_remap(cache: KVCache, layer0: int, n_layers: int, sel, block_table, phys,
+                     miss_page, miss_slot, n_miss, status, ws, stream=None):
+    """ssa_ensure_resident that also writes the remapped table (one launch fewer)."""
+    _check(lib().ssa_ensure_remap(ctypes.byref(cache._lay), ctypes.byref(cache.c), layer0,
+                                  n_layers, _ptr(sel), _ptr(block_table), _ptr(phys),
+                                  _ptr(miss_page), _ptr(miss_slot), _ptr(n_miss), _ptr(status),
+                                  _ptr(ws), _stream(stream)))
+
+
+def ssa_prefetch_pages(cache: KVCache, layer0: int, n_layers: int, scores, block_table,
+                       seq_lens, width: int, fetch_page, fetch_slot, n_fetch, status, ws,
+                       stream=None):
+    """Top-k preload after a step's ensure: fetch the top (width-1) pages plus
+    the last page of each request by that step's scores ahead of the next."""
+    _check(lib().ssa_prefetch_pages(ctypes.byref(cache._lay), ctypes.byref(cache.c), layer0,
+                                    n_layers, _ptr(scores), _ptr(block_table), _ptr(seq_lens),
+                                    int(width), _ptr(fetch_page), _ptr(fetch_slot),
+                                    _ptr(n_fetch), _ptr(status), _ptr(ws), _stream(stream)))
+
+
 def ssa_remap_block_table(cache: KVCache, layer0: int, n_layers: int, sel, block_table, phys,
                           status, stream=None):
     _check(lib().ssa_remap_block_table(ctypes.byref(cache._lay), ctypes.byref(cache.c), layer0,
@@ -251,6 +283,17 @@ def ssa_sparse_paged_decode(cache: KVCache, layer0: int, n_layers: int, q, sel, 
                                          n_layers, _ptr(q), _ptr(sel), _ptr(phys),
                                          _ptr(seq_lens), float(sm_scale), _ptr(out),
                                          _ptr(status), _ptr(ws), _stream(stream)))
+
+
+def ssa_sparse_paged_decode_host_tail(cache: KVCache, layer0: int, n_layers: int, q, sel,
+                                      block_table, seq_lens, sm_scale: float, out, status, ws,
+                                      stream=None):
+    """Attention over the selected pages, non-resident ones read straight from
+    the pinned host mirror (no ensure, no copy)."""
+    _check(lib().ssa_sparse_paged_decode_host_tail(
+        ctypes.byref(cache._lay), ctypes.byref(cache.c), layer0, n_layers, _ptr(q), _ptr(sel),
+        _ptr(block_table), _ptr(seq_lens), float(sm_scale), _ptr(out), _ptr(status), _ptr(ws),
+        _stream(stream)))
 
 
 def ssa_selftest_bounded_wait(status, stream=None):

@@ -83,7 +83,9 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // layout.  Only the tickets need a defined start (zero); every call leaves
 // them zero.
 struct WsLayout {
-  size_t scores, miss_page, miss_slot, n_miss, part_o, part_ml, tickets, idx_tickets, total;
+  size_t scores, miss_page, miss_slot, n_miss, part_o, part_ml, tickets, idx_tickets;
+  size_t pf_cand, pf_ncand, pf_miss_page, pf_miss_slot, pf_n_miss;   // ssa_prefetch_pages
+  size_t total;
 };
 
 size_t part_entries(const Dims& d) {
@@ -102,6 +104,11 @@ WsLayout ws_layout(const Dims& d) {
   w.part_ml = off;   off += align256(pe * 2 * 4);
   w.tickets = off;   off += align256((size_t)d.Lyr * d.B * d.Hkv * 4);
   w.idx_tickets = off; off += align256((size_t)d.Lyr * d.B * 4);
+  w.pf_cand = off;   off += align256((size_t)d.Lyr * d.B * d.W * 4);
+  w.pf_ncand = off;  off += align256((size_t)d.Lyr * d.B * 4);
+  w.pf_miss_page = off; off += align256((size_t)d.Lyr * d.B * d.W * 4);
+  w.pf_miss_slot = off; off += align256((size_t)d.Lyr * d.B * d.W * 4);
+  w.pf_n_miss = off; off += align256((size_t)d.Lyr * 4);
   w.total = off;
   return w;
 }
@@ -207,10 +214,10 @@ int ssa_index_topk(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_
   return e == cudaSuccess ? SSA_OK : fail_cuda(e);
 }
 
-int ssa_ensure_resident(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
-                        const int32_t* sel, const int32_t* block_table,
-                        int32_t* miss_page_opt, int32_t* miss_slot_opt, int32_t* n_miss_opt,
-                        int32_t* status, void* ws, ssa_stream_t stream) {
+static int ensure_impl(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                       const int32_t* sel, const int32_t* block_table, int32_t* miss_page_opt,
+                       int32_t* miss_slot_opt, int32_t* n_miss_opt, int32_t* phys_opt,
+                       int32_t* status, void* ws, ssa_stream_t stream) {
   Dims d;
   int r = check_layout(lay, d);
   if (r) return r;
@@ -226,7 +233,57 @@ int ssa_ensure_resident(const ssa_layout* lay, const ssa_cache* c, int layer0, i
   int32_t* nm = n_miss_opt ? n_miss_opt : at<int32_t>(ws, w.n_miss);
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = launch_ensure_state(d, *c, layer0, n_layers, sel, block_table, mp, ms, nm,
-                                      status, s);
+                                      phys_opt, status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_miss_copy(d, *c, layer0, n_layers, mp, ms, nm, status, s);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
+int ssa_ensure_resident(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                        const int32_t* sel, const int32_t* block_table,
+                        int32_t* miss_page_opt, int32_t* miss_slot_opt, int32_t* n_miss_opt,
+                        int32_t* status, void* ws, ssa_stream_t stream) {
+  return ensure_impl(lay, c, layer0, n_layers, sel, block_table, miss_page_opt, miss_slot_opt,
+                     n_miss_opt, nullptr, status, ws, stream);
+}
+
+int ssa_ensure_remap(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                     const int32_t* sel, const int32_t* block_table, int32_t* phys,
+                     int32_t* miss_page_opt, int32_t* miss_slot_opt, int32_t* n_miss_opt,
+                     int32_t* status, void* ws, ssa_stream_t stream) {
+  if (!phys) return SSA_ERR_INVALID_ARG;
+  return ensure_impl(lay, c, layer0, n_layers, sel, block_table, miss_page_opt, miss_slot_opt,
+                     n_miss_opt, phys, status, ws, stream);
+}
+
+int ssa_prefetch_pages(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                       const int32_t* scores, const int32_t* block_table, const int32_t* seq_lens,
+                       int width, int32_t* fetch_page_opt, int32_t* fetch_slot_opt,
+                       int32_t* n_fetch_opt, int32_t* status, void* ws, ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if ((r = check_cache(d, c))) return r;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (!scores || !block_table || !seq_lens || !ws) return SSA_ERR_INVALID_ARG;
+  if (width < 1 || width > d.W) return SSA_ERR_INVALID_ARG;
+  const long long need = (long long)d.B * d.W < d.Lp ? (long long)d.B * d.W : d.Lp;
+  if (d.S < need) return SSA_ERR_POOL_TOO_SMALL;
+  const WsLayout w = ws_layout(d);
+  int32_t* cand = at<int32_t>(ws, w.pf_cand);
+  int32_t* mp = fetch_page_opt ? fetch_page_opt : at<int32_t>(ws, w.pf_miss_page);
+  int32_t* ms = fetch_slot_opt ? fetch_slot_opt : at<int32_t>(ws, w.pf_miss_slot);
+  int32_t* nm = n_fetch_opt ? n_fetch_opt : at<int32_t>(ws, w.pf_n_miss);
+  cudaStream_t s = (cudaStream_t)stream;
+  // the candidates: the selection rule with k = width - 1 over the step's scores
+  Dims dw = d;
+  dw.k = width - 1;
+  dw.W = width;
+  cudaError_t e = launch_topk_select(dw, n_layers, scores, seq_lens, cand,
+                                     at<int32_t>(ws, w.pf_ncand), status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_preload_state(d, *c, layer0, n_layers, cand, width, block_table, mp, ms, nm, status,
+                           s);
   if (e != cudaSuccess) return fail_cuda(e);
   e = launch_miss_copy(d, *c, layer0, n_layers, mp, ms, nm, status, s);
   return e == cudaSuccess ? SSA_OK : fail_cuda(e);
@@ -246,18 +303,23 @@ int ssa_remap_block_table(const ssa_layout* lay, const ssa_cache* c, int layer0,
   return e == cudaSuccess ? SSA_OK : fail_cuda(e);
 }
 
-int ssa_sparse_paged_decode(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
-                            const void* q, const int32_t* sel, const int32_t* phys,
-                            const int32_t* seq_lens, float sm_scale, void* out,
-                            int32_t* status, void* ws, ssa_stream_t stream) {
+static int decode_impl(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                       const void* q, const int32_t* sel, const int32_t* phys,
+                       const int32_t* block_table, const int32_t* seq_lens, float sm_scale,
+                       void* out, int32_t* status, void* ws, ssa_stream_t stream) {
   Dims d;
   int r = check_layout(lay, d);
   if (r) return r;
   if (!c || !c->k_pool || !c->v_pool || (d.fp8 && (!c->k_scale || !c->v_scale)))
     return SSA_ERR_INVALID_ARG;
   if ((r = check_range(d, layer0, n_layers))) return r;
-  if (!q || !sel || !phys || !seq_lens || !out) return SSA_ERR_INVALID_ARG;
+  const bool host_tail = block_table != nullptr;
+  if (!q || !sel || (!phys && !host_tail) || !seq_lens || !out) return SSA_ERR_INVALID_ARG;
   if (!ws) return SSA_ERR_INVALID_ARG;
+  if (host_tail) {
+    if (!c->slot_of) return SSA_ERR_INVALID_ARG;
+    if (!mirror_consistent(d, c) || !has_mirror(d, c)) return SSA_ERR_NO_MIRROR;
+  }
   const WsLayout w = ws_layout(d);
   DecodeArgs a{};
   a.d = &d;
@@ -275,8 +337,28 @@ int ssa_sparse_paged_decode(const ssa_layout* lay, const ssa_cache* c, int layer
   a.part_ml = at<float>(ws, w.part_ml);
   a.tickets = at<int32_t>(ws, w.tickets);
   a.status = status;
+  a.host_tail = host_tail ? 1 : 0;
+  a.bt = block_table;
   cudaError_t e = launch_decode(a, (cudaStream_t)stream);
   return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
+int ssa_sparse_paged_decode(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                            const void* q, const int32_t* sel, const int32_t* phys,
+                            const int32_t* seq_lens, float sm_scale, void* out,
+                            int32_t* status, void* ws, ssa_stream_t stream) {
+  return decode_impl(lay, c, layer0, n_layers, q, sel, phys, nullptr, seq_lens, sm_scale, out,
+                     status, ws, stream);
+}
+
+int ssa_sparse_paged_decode_host_tail(const ssa_layout* lay, const ssa_cache* c, int layer0,
+                                      int n_layers, const void* q, const int32_t* sel,
+                                      const int32_t* block_table, const int32_t* seq_lens,
+                                      float sm_scale, void* out, int32_t* status, void* ws,
+                                      ssa_stream_t stream) {
+  if (!block_table) return SSA_ERR_INVALID_ARG;
+  return decode_impl(lay, c, layer0, n_layers, q, sel, nullptr, block_table, seq_lens, sm_scale,
+                     out, status, ws, stream);
 }
 
 const char* ssa_status_str(int code) {
@@ -295,8 +377,8 @@ const char* ssa_status_str(int code) {
     static thread_local char buf[256];
     buf[0] = 0;
     const char* names[] = {"drop", "bad_id", "miss_no_mirror", "unresolved", "bad_pos",
-                           "timeout"};
-    for (int i = 0; i < 6; ++i)
+                           "timeout", "internal"};
+    for (int i = 0; i < 7; ++i)
       if (code & (1 << i)) {
         if (buf[0]) strncat(buf, "|", sizeof(buf) - strlen(buf) - 1);
         strncat(buf, names[i], sizeof(buf) - strlen(buf) - 1);

@@ -1,12 +1,13 @@
 // ensure.cu -- a3 LRU ensure, a4 miss fetch, a5 block-table remap.
 //
-// FreeToken PR #499, "What": the GPU pool is an LRU cache of physical slots
-// over the logical page space, backed by the pinned host mirror.  "Design":
-// lru_ensure is a device-side LRU with fixed shapes (graph-safe, no host
-// sync, no data-dependent shapes); eviction is a pure rebind because slots
-// are drop-clean; fast_index_copy moves K+V of each miss host -> device.
-// FreeToken PR #525: the copy carries the per-token scale banks, and the
-// whole batch selection fits the pool by construction.
+// FreeToken PR #499, "What" and "Design": the GPU's slots cache logical
+// pages whose full copy lives in pinned host memory; the least recently used
+// slot is reused first.  The update has fixed shapes and no host round trip,
+// so a step can be captured in a CUDA graph; since the host copy is always
+// current, evicting a page only rebinds its slot; each miss's K and V are
+// then copied host -> device.  FreeToken PR #525: the copy includes the
+// per-token fp8 scales, and the pool is sized so that a batch's whole
+// selection fits.
 //
 // Order of events per layer (the pages state none; this is the reading the
 // library takes, identical in the oracle):
@@ -49,20 +50,28 @@ __device__ void bitonic_sort_smem(T* a, int n /* power of two */) {
 
 struct EnsureParams {
   int32_t *slot_of, *page_of, *last_use, *clock;
-  const int32_t* sel;    // [n_layers][B][W]
+  const int32_t* sel;    // [n_layers][B][W] page indices (W: the entries per request)
   const int32_t* bt;     // [B][nmax]
-  int32_t* miss_page;    // [n_layers][B*W]
+  int32_t* miss_page;    // [n_layers][mstride]
   int32_t* miss_slot;
   int32_t* n_miss;       // [n_layers]
+  int32_t* phys;         // [n_layers][B][W] or null: the remapped table (a5 fused)
   int32_t* status;
-  int layer0, Lp, S, B, W, nmax, N2;
+  int layer0, Lp, S, B, W, nmax, N2, mstride;
   int has_mirror;
+  // 0: the step's ensure (epoch = clock; hits touched; every miss bound; clock
+  // advances).  1: a preload after the step's ensure (epoch = clock - 1;
+  // slots of that epoch are never victims; misses beyond the victims left
+  // are not fetched; the clock stays).
+  int preload;
 };
 
+// Order-preserving victim key of slot s: 0xFFFFFFFF for a slot of the
+// current epoch (never a victim), free slots first, then by last_use.
 __device__ __forceinline__ uint32_t victim_key(const int32_t* page_of, const int32_t* last_use,
-                                               int s, int32_t clock) {
+                                               int s, int32_t epoch) {
   const int32_t po = page_of[s], lu = last_use[s];
-  if (po >= 0 && lu == clock) return 0xFFFFFFFFu;             // touched this step: a hit
+  if (po >= 0 && lu == epoch) return 0xFFFFFFFFu;             // touched this epoch
   const int32_t k = po < 0 ? -2 : lu;                          // free slots first
   return (uint32_t)k ^ 0x80000000u;
 }
@@ -87,7 +96,7 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
   __shared__ int hist[256];
   __shared__ int tmp[33];
   __shared__ uint32_t s_prefix, s_lo, s_hi;
-  __shared__ int s_remaining, s_nv;
+  __shared__ int s_remaining, s_nv, s_ncand;
   pdl_trigger();
   pdl_wait();
 
@@ -97,9 +106,11 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
   int32_t* slot_of = p.slot_of + (size_t)layer * p.Lp;
   int32_t* page_of = p.page_of + (size_t)layer * p.S;
   int32_t* last_use = p.last_use + (size_t)layer * p.S;
-  int32_t* mpage = p.miss_page + (size_t)li * BW;
-  int32_t* mslot = p.miss_slot + (size_t)li * BW;
-  const int32_t clock = p.clock[layer];
+  int32_t* mpage = p.miss_page + (size_t)li * p.mstride;
+  int32_t* mslot = p.miss_slot + (size_t)li * p.mstride;
+  // the epoch whose slots are never victims, and the last_use given to the
+  // ids this call touches or binds
+  const int32_t clock = p.clock[layer] - (p.preload ? 1 : 0);
 
   // 1. the distinct selected logical ids, ascending, in ids[] (0xFFFFFFFF
   //    after them)
@@ -182,128 +193,157 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
     // bins over the range need one or two passes where the full 32 bits
     // need four
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    int ncand = 0;
     for (int s = tid; s < p.S; s += nt) {
       const uint32_t kk = key_of(s);
-      if (kk != 0xFFFFFFFFu) { lo = min(lo, kk); hi = max(hi, kk); }
+      if (kk != 0xFFFFFFFFu) { lo = min(lo, kk); hi = max(hi, kk); ++ncand; }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
       hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      ncand += __shfl_xor_sync(0xffffffffu, ncand, o);
     }
-    if (tid == 0) { s_lo = 0xFFFFFFFFu; s_hi = 0u; s_remaining = m; s_nv = 0; }
+    if (tid == 0) { s_lo = 0xFFFFFFFFu; s_hi = 0u; s_nv = 0; s_ncand = 0; }
     __syncthreads();
-    if ((tid & 31) == 0) { atomicMin(&s_lo, lo); atomicMax(&s_hi, hi); }
+    if ((tid & 31) == 0) { atomicMin(&s_lo, lo); atomicMax(&s_hi, hi); atomicAdd(&s_ncand, ncand); }
     __syncthreads();
-    // LSB-side radix search for the m-th smallest key within [base, span_hi]:
-    // bins of 8 bits of (key - base), from the highest bit the range uses
-    uint32_t base = s_lo, span_hi = s_hi;
-    const uint32_t range = s_hi - s_lo;
-    int shift = range == 0 ? 0 : max(0, 32 - __clz((int)range) - 8);
-    if (range >> 31) shift = 24;
-    for (;;) {
-      for (int i = tid; i < 256; i += nt) hist[i] = 0;
-      __syncthreads();
-      for (int b0 = 0; b0 < p.S; b0 += nt) {        // uniform trip count
-        const int s = b0 + tid;
-        const uint32_t kk = s < p.S ? key_of(s) : 0xFFFFFFFFu;
-        const bool use = s < p.S && kk >= base && kk <= span_hi && kk != 0xFFFFFFFFu;
-        // one atomic per distinct bin per warp: last_use values cluster
-        const int key = use ? (int)(((kk - base) >> shift) & 255) : -1 - (tid & 31);
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        if (use && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[key], __popc(peers));
-      }
-      __syncthreads();
-      if (tid < 32) {
-        int cnt[8], sum = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) { cnt[j] = hist[8 * tid + j]; sum += cnt[j]; }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (tid >= o) incl += y;
+    // a preload fetches the first misses (ascending id) that find a victim;
+    // the ensure's capacity rule leaves it a victim for every miss
+    if (s_ncand < m) {
+      for (int i = s_ncand + tid; i < m; i += nt) mpage[i] = -1;
+      m = s_ncand;
+    }
+    if (tid == 0) s_remaining = m;
+    __syncthreads();
+    if (m > 0) {
+      // LSB-side radix search for the m-th smallest key within [base, span_hi]:
+      // bins of 8 bits of (key - base), from the highest bit the range uses
+      uint32_t base = s_lo, span_hi = s_hi;
+      const uint32_t range = s_hi - s_lo;
+      int shift = range == 0 ? 0 : max(0, 32 - __clz((int)range) - 8);
+      if (range >> 31) shift = 24;
+      for (;;) {
+        for (int i = tid; i < 256; i += nt) hist[i] = 0;
+        __syncthreads();
+        for (int b0 = 0; b0 < p.S; b0 += nt) {        // uniform trip count
+          const int s = b0 + tid;
+          const uint32_t kk = s < p.S ? key_of(s) : 0xFFFFFFFFu;
+          const bool use = s < p.S && kk >= base && kk <= span_hi && kk != 0xFFFFFFFFu;
+          // one atomic per distinct bin per warp: last_use values cluster
+          const int key = use ? (int)(((kk - base) >> shift) & 255) : -1 - (tid & 31);
+          const unsigned peers = __match_any_sync(0xffffffffu, key);
+          if (use && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[key], __popc(peers));
         }
-        const int rem = s_remaining;
-        const unsigned hit = __ballot_sync(0xffffffffu, incl >= rem);
-        const int lane = __ffs(hit) - 1;
-        if (tid == lane) {
-          int below = incl - sum;
-          for (int j = 0; j < 8; ++j) {
-            if (below + cnt[j] >= rem) {
-              s_remaining = rem - below;
-              s_prefix = base + ((uint32_t)(8 * tid + j) << shift);
-              break;
+        __syncthreads();
+        if (tid < 32) {
+          int cnt[8], sum = 0;
+  #pragma unroll
+          for (int j = 0; j < 8; ++j) { cnt[j] = hist[8 * tid + j]; sum += cnt[j]; }
+          int incl = sum;
+  #pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (tid >= o) incl += y;
+          }
+          const int rem = s_remaining;
+          const unsigned hit = __ballot_sync(0xffffffffu, incl >= rem);
+          const int lane = __ffs(hit) - 1;
+          if (tid == lane) {
+            int below = incl - sum;
+            for (int j = 0; j < 8; ++j) {
+              if (below + cnt[j] >= rem) {
+                s_remaining = rem - below;
+                s_prefix = base + ((uint32_t)(8 * tid + j) << shift);
+                break;
+              }
+              below += cnt[j];
             }
-            below += cnt[j];
           }
         }
+        __syncthreads();
+        base = s_prefix;
+        if (shift == 0) break;
+        span_hi = (uint32_t)min((unsigned long long)base + ((1ull << shift) - 1ull), 0xFFFFFFFEull);
+        shift = shift >= 8 ? shift - 8 : 0;
+      }
+      const uint32_t T = s_prefix;
+      const int need_eq = s_remaining;
+      // gather: keys below T (any order), then the need_eq lowest slots equal to T
+      const int sper = (p.S + nt - 1) / nt;
+      const int s0 = min(p.S, tid * sper), s1 = min(p.S, s0 + sper);
+      int eq = 0;
+      for (int s = s0; s < s1; ++s) {
+        const uint32_t kk = key_of(s);
+        if (kk < T) vic[atomicAdd(&s_nv, 1)] = ((uint64_t)kk << 32) | (uint32_t)s;
+        else if (kk == T) ++eq;
+      }
+      int eqtot;
+      int er = block_exclusive_scan(eq, tmp, eqtot);
+      const int n_lt = m - need_eq;
+      for (int s = s0; s < s1 && er < need_eq; ++s) {
+        const uint32_t kk = key_of(s);
+        if (kk == T) {
+          if (er < need_eq) vic[n_lt + er] = ((uint64_t)kk << 32) | (uint32_t)s;
+          ++er;
+        }
       }
       __syncthreads();
-      base = s_prefix;
-      if (shift == 0) break;
-      span_hi = (uint32_t)min((unsigned long long)base + ((1ull << shift) - 1ull), 0xFFFFFFFEull);
-      shift = shift >= 8 ? shift - 8 : 0;
-    }
-    const uint32_t T = s_prefix;
-    const int need_eq = s_remaining;
-    // gather: keys below T (any order), then the need_eq lowest slots equal to T
-    const int sper = (p.S + nt - 1) / nt;
-    const int s0 = min(p.S, tid * sper), s1 = min(p.S, s0 + sper);
-    int eq = 0;
-    for (int s = s0; s < s1; ++s) {
-      const uint32_t kk = key_of(s);
-      if (kk < T) vic[atomicAdd(&s_nv, 1)] = ((uint64_t)kk << 32) | (uint32_t)s;
-      else if (kk == T) ++eq;
-    }
-    int eqtot;
-    int er = block_exclusive_scan(eq, tmp, eqtot);
-    const int n_lt = m - need_eq;
-    for (int s = s0; s < s1 && er < need_eq; ++s) {
-      const uint32_t kk = key_of(s);
-      if (kk == T) {
-        if (er < need_eq) vic[n_lt + er] = ((uint64_t)kk << 32) | (uint32_t)s;
-        ++er;
+      // 4. victim order: (key, slot) ascending.  The keys are distinct (slots
+      //    are), so each victim's rank is the count of smaller keys.
+      if (m <= kRankMax) {
+        for (int i = tid; i < m; i += nt) {
+          const uint64_t x = vic[i];
+          int r = 0;
+          for (int j = 0; j < m; ++j) r += vic[j] < x;
+          ids[r] = (uint32_t)(x & 0xFFFFFFFFu);      // ids are no longer needed
+        }
+      } else {
+        int M2 = 1;
+        while (M2 < m) M2 <<= 1;
+        for (int i = m + tid; i < M2; i += nt) vic[i] = ~0ull;
+        __syncthreads();
+        bitonic_sort_smem(vic, M2);
+        for (int i = tid; i < m; i += nt) ids[i] = (uint32_t)(vic[i] & 0xFFFFFFFFu);
       }
-    }
-    __syncthreads();
-    // 4. victim order: (key, slot) ascending.  The keys are distinct (slots
-    //    are), so each victim's rank is the count of smaller keys.
-    if (m <= kRankMax) {
-      for (int i = tid; i < m; i += nt) {
-        const uint64_t x = vic[i];
-        int r = 0;
-        for (int j = 0; j < m; ++j) r += vic[j] < x;
-        ids[r] = (uint32_t)(x & 0xFFFFFFFFu);      // ids are no longer needed
-      }
-    } else {
-      int M2 = 1;
-      while (M2 < m) M2 <<= 1;
-      for (int i = m + tid; i < M2; i += nt) vic[i] = ~0ull;
       __syncthreads();
-      bitonic_sort_smem(vic, M2);
-      for (int i = tid; i < m; i += nt) ids[i] = (uint32_t)(vic[i] & 0xFFFFFFFFu);
-    }
-    __syncthreads();
 
-    // 5. rebind: i-th miss takes the i-th victim
-    for (int i = tid; i < m; i += nt) {
-      const int pg = mpage[i];
-      const int v = (int)ids[i];
-      const int old = page_of[v];
-      if (old >= 0 && old < p.Lp) slot_of[old] = -1;
-      slot_of[pg] = v;
-      page_of[v] = pg;
-      last_use[v] = clock;
-      mslot[i] = v;
+      // 5. rebind: i-th miss takes the i-th victim
+      for (int i = tid; i < m; i += nt) {
+        const int pg = mpage[i];
+        const int v = (int)ids[i];
+        const int old = page_of[v];
+        if (old >= 0 && old < p.Lp) slot_of[old] = -1;
+        slot_of[pg] = v;
+        page_of[v] = pg;
+        last_use[v] = clock;
+        mslot[i] = v;
+      }
     }
-    if (tid == 0 && !p.has_mirror) set_status(p.status, SSA_ST_MISS_NO_MIRROR);
+    if (tid == 0 && m > 0 && !p.has_mirror) set_status(p.status, SSA_ST_MISS_NO_MIRROR);
   }
-  for (int i = m + tid; i < BW; i += nt) { mpage[i] = -1; mslot[i] = -1; }
+  for (int i = m + tid; i < p.mstride; i += nt) { mpage[i] = -1; mslot[i] = -1; }
   __syncthreads();
   if (tid == 0) {
     p.n_miss[li] = m;
-    p.clock[layer] = clock + 1;
+    if (!p.preload) p.clock[layer] = clock + 1;
+  }
+  if (p.phys) {
+    // a5 fused: every selected page of the layer now has its slot (the
+    // rebind above is visible block-wide), so translate the table here
+    int32_t* phys = p.phys + (size_t)li * BW;
+    const int32_t* sel = p.sel + (size_t)li * BW;
+    for (int i = tid; i < BW; i += nt) {
+      const int b = i / p.W;
+      const int pg = sel[i];
+      int out = -1;
+      if (pg >= 0) {
+        const int id = pg < p.nmax ? p.bt[(size_t)b * p.nmax + pg] : -1;
+        if (id >= 0 && id < p.Lp) out = slot_of[id];
+        if (out < 0) set_status(p.status, SSA_ST_UNRESOLVED);
+      }
+      phys[i] = out;
+    }
   }
 }
 
@@ -408,16 +448,21 @@ int ensure_sort_width(const Dims& d) {
   return n;
 }
 
-cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
-                                const int32_t* sel, const int32_t* bt, int32_t* miss_page,
-                                int32_t* miss_slot, int32_t* n_miss, int32_t* status,
-                                cudaStream_t s) {
+namespace {
+
+cudaError_t launch_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                         const int32_t* sel, int width, int preload, const int32_t* bt,
+                         int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
+                         int32_t* phys, int32_t* status, cudaStream_t s) {
   EnsureParams p{};
+  p.phys = phys;
   p.slot_of = c.slot_of; p.page_of = c.page_of; p.last_use = c.last_use; p.clock = c.clock;
   p.sel = sel; p.bt = bt; p.miss_page = miss_page; p.miss_slot = miss_slot; p.n_miss = n_miss;
   p.status = status;
-  p.layer0 = layer0; p.Lp = d.Lp; p.S = d.S; p.B = d.B; p.W = d.W; p.nmax = d.nmax;
+  p.layer0 = layer0; p.Lp = d.Lp; p.S = d.S; p.B = d.B; p.W = width; p.nmax = d.nmax;
   p.N2 = ensure_sort_width(d);
+  p.mstride = d.B * d.W;
+  p.preload = preload;
   p.has_mirror = c.k_mirror != nullptr;
   // small batches and pools: 256 threads (cheaper barriers); else 1024
   const int threads = (p.N2 <= 1024 && d.S <= 4096) ? 256 : kEnsureThreads;
@@ -430,13 +475,32 @@ cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, i
       d.S <= kSmemKeys && with_keys + kEnsureStaticSmem <= (size_t)current_device_info().smem_optin;
   const size_t smem = keys_in_smem ? with_keys : base;
   auto k = keys_in_smem ? ensure_state_kernel<true> : ensure_state_kernel<false>;
-  if (smem > 48 * 1024) {
+  // the default limit (48 KiB) covers static and dynamic shared memory together
+  if (smem + kEnsureStaticSmem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = launch_pdl(k, dim3(n_layers), dim3(threads), smem, s, p);
   count_launch();
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                                const int32_t* sel, const int32_t* bt, int32_t* miss_page,
+                                int32_t* miss_slot, int32_t* n_miss, int32_t* phys,
+                                int32_t* status, cudaStream_t s) {
+  return launch_state(d, c, layer0, n_layers, sel, d.W, 0, bt, miss_page, miss_slot, n_miss,
+                      phys, status, s);
+}
+
+cudaError_t launch_preload_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                                 const int32_t* cand, int width, const int32_t* bt,
+                                 int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
+                                 int32_t* status, cudaStream_t s) {
+  return launch_state(d, c, layer0, n_layers, cand, width, 1, bt, miss_page, miss_slot, n_miss,
+                      nullptr, status, s);
 }
 
 cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int n_layers,

@@ -182,6 +182,9 @@ __global__ void __launch_bounds__(kScoreThreads, CPL == 1 ? 3 : 2) index_score_k
 // top-k select: one CTA per (layer, request)
 // ---------------------------------------------------------------------------
 constexpr int kSelThreads = 1024;
+// Upper bound on the static shared memory of the select (and fused index)
+// kernels: histogram, scan scratch, a few scalars.
+constexpr size_t kSelectStaticSmem = 2048;
 
 struct SelectParams {
   const int32_t* scores;   // [n_layers][B][nmax]
@@ -450,13 +453,13 @@ cudaError_t launch_index_topk(const Dims& d, const ssa_cache& c, int layer0, int
   p.pages_per_cta = score_pages_per_cta(d, n_layers, p.lanes, occ);
   dim3 grid((d.nmax + p.pages_per_cta - 1) / p.pages_per_cta, d.B, n_layers);
   if (cpl == 1) {
-    if (smem > 48 * 1024 &&
+    if (smem + kSelectStaticSmem > 48 * 1024 &&
         (e = cudaFuncSetAttribute(index_topk_kernel<1>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
       return e;
     e = launch_pdl(index_topk_kernel<1>, grid, dim3(kScoreThreads), smem, s, f);
   } else {
-    if (smem > 48 * 1024 &&
+    if (smem + kSelectStaticSmem > 48 * 1024 &&
         (e = cudaFuncSetAttribute(index_topk_kernel<2>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
       return e;
@@ -471,7 +474,7 @@ cudaError_t launch_topk_select(const Dims& d, int n_layers, const int32_t* score
                                int32_t* status, cudaStream_t s) {
   SelectParams p{scores, seq_lens, sel, n_sel, status, d.B, d.nmax, d.P, d.k, d.W};
   const size_t smem = (size_t)d.nmax * sizeof(uint32_t);
-  if (smem > 48 * 1024) {
+  if (smem + kSelectStaticSmem > 48 * 1024) {   // the default limit counts static memory too
     cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -44,10 +44,17 @@ cudaError_t launch_topk_select(const Dims& d, int n_layers, const int32_t* score
                                int32_t* status, cudaStream_t s);
 
 // -- ensure.cu --------------------------------------------------------------
+// phys: null, or [n_layers][B][W] to receive the remapped table (a5 fused)
 cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
                                 const int32_t* sel, const int32_t* bt, int32_t* miss_page,
-                                int32_t* miss_slot, int32_t* n_miss, int32_t* status,
-                                cudaStream_t s);
+                                int32_t* miss_slot, int32_t* n_miss, int32_t* phys,
+                                int32_t* status, cudaStream_t s);
+// The preload's state update: candidates cand [n_layers][B][width] (page
+// indices, -1 padded) after a step's ensure; epoch clock - 1, the clock stays.
+cudaError_t launch_preload_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
+                                 const int32_t* cand, int width, const int32_t* bt,
+                                 int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
+                                 int32_t* status, cudaStream_t s);
 cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
                              const int32_t* miss_page, const int32_t* miss_slot,
                              const int32_t* n_miss, int32_t* status, cudaStream_t s);
@@ -70,6 +77,10 @@ struct DecodeArgs {
   float* part_ml;  // [decode_max_ctas][2][G][2]
   int32_t* tickets;  // [units] piece counters (zero before the first call; left zero)
   int32_t* status;
+  // host-tail mode: phys unused; pages resolved through slot_of, those
+  // without a slot read from the mirror
+  int host_tail;
+  const int32_t* bt;  // [B][nmax]
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 

@@ -1,11 +1,11 @@
 // store.cu -- a0: store K/V through the write-through host mirror, update the
 // indexer slab; and the residency-state reset.
 //
-// FreeToken PR #499, "Design": every store is mirrored to a pinned host bank
-// over UVA, so a GPU slot is always drop-clean and eviction is a pure rebind.
-// FreeToken PR #525 (mirror_store_quant): for an fp8 pool the mirror receives
-// the e4m3 codes and fp32 scales AFTER quantisation -- the pool is the source
-// of truth and the two hold identical bytes.
+// FreeToken PR #499, "Design": each stored token is also written to pinned
+// host memory (over unified addressing), so evicting a slot never needs a
+// write-back.  FreeToken PR #525 (mirror_store_quant): with fp8 the host copy
+// receives the quantised e4m3 codes and their fp32 scales, so host copy and
+// pool hold the same bytes.
 //
 // One CTA per run of consecutive tokens of one logical page (the CTA of the
 // run's first token does the work; every other CTA returns at once), so the

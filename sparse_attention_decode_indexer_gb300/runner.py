@@ -1,13 +1,20 @@
 """DecodeRunner: the decode step over a layer range, as a user calls it.
 
 Holds the cache, the per-step device buffers and the workspace, and issues the
-four calls of one decode step (index + select, ensure, remap, attention) on
-the current stream.  Two launch modes:
+calls of one decode step (index + select, ensure, remap, attention) on the
+current stream.  Two launch modes:
   * layer-batched (default): each call covers all layers of the range in one
     launch -- valid whenever every layer's query is known before the step;
   * per-layer: the four calls per layer, layer after layer, as a model whose
     next layer's query depends on this layer's output must run them.
 No call synchronises the host, so a whole step can be captured in a CUDA graph.
+
+With ``preload_width`` > 0 (layer-batched steps), every step also issues the
+top-k preload (ssa_prefetch_pages) on a second stream once its remap is done:
+the next step's likely pages are fetched while this step's attention and the
+next step's indexer run, and the next step's ensure waits for it.  The
+step's scores alternate between two buffers so that the preload reads one
+while the next indexer writes the other.
 """
 from __future__ import annotations
 
@@ -15,14 +22,14 @@ import math
 
 import torch
 
-from . import (KVCache, Layout, ssa_ensure_resident, ssa_index_topk, ssa_lru_init,
-               ssa_remap_block_table, ssa_sparse_paged_decode, ssa_store_kv_mirror,
-               ssa_workspace_size)
+from . import (KVCache, Layout, ssa_ensure_remap, ssa_ensure_resident, ssa_index_topk,
+               ssa_lru_init, ssa_prefetch_pages, ssa_remap_block_table, ssa_sparse_paged_decode,
+               ssa_store_kv_mirror, ssa_workspace_size)
 
 
 class DecodeRunner:
     def __init__(self, layout: Layout, host_tier: bool, identity: bool, block_table, seq_lens,
-                 device="cuda"):
+                 device="cuda", preload_width: int = 0):
         self.layout = layout
         self.cache = KVCache(layout, host_tier, device)
         L, B, W = layout.n_layers, layout.batch, layout.max_sel
@@ -44,6 +51,26 @@ class DecodeRunner:
                               device=device)
         self.sm_scale = 1.0 / math.sqrt(layout.head_dim)
         ssa_lru_init(self.cache, identity)
+        self.preload_width = 0
+        if preload_width:
+            self.enable_preload(preload_width)
+
+    def enable_preload(self, width: int):
+        """Issue the top-k preload of `width` pages per request with every
+        later layer-batched step (0 turns it off)."""
+        self.preload_width = int(width)
+        if not self.preload_width or hasattr(self, "side"):
+            return
+        L, B, W = self.layout.n_layers, self.layout.batch, self.layout.max_sel
+        dev, i32 = self.scores.device, torch.int32
+        self.scores_alt = torch.zeros_like(self.scores)
+        self.fetch_page = torch.full((L, B * W), -1, dtype=i32, device=dev)
+        self.fetch_slot = torch.full((L, B * W), -1, dtype=i32, device=dev)
+        self.n_fetch = torch.zeros((L,), dtype=i32, device=dev)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_remap = torch.cuda.Event()
+        self.ev_preload = torch.cuda.Event()
+        self.n_steps = 0
 
     # write path ---------------------------------------------------------------
     def store(self, layer0: int, n_layers: int, k, v, pos):
@@ -51,26 +78,55 @@ class DecodeRunner:
         ssa_store_kv_mirror(self.cache, layer0, n_layers, k, v, pos, self.status)
 
     # one decode step ------------------------------------------------------------
-    def _calls(self, q, layer0: int, n_layers: int, keep_scores: bool):
+    def _calls(self, q, layer0: int, n_layers: int, keep_scores: bool, fused: bool):
         sl = slice(layer0, layer0 + n_layers)
         c = self.cache
         ssa_index_topk(c, layer0, n_layers, q, self.block_table, self.seq_lens, self.sel[sl],
                        self.n_sel[sl], self.scores[sl] if keep_scores else None, self.status,
                        self.ws)
-        ssa_ensure_resident(c, layer0, n_layers, self.sel[sl], self.block_table,
-                            self.miss_page[sl], self.miss_slot[sl], self.n_miss[sl], self.status,
-                            self.ws)
-        ssa_remap_block_table(c, layer0, n_layers, self.sel[sl], self.block_table, self.phys[sl],
-                              self.status)
+        if fused:
+            ssa_ensure_remap(c, layer0, n_layers, self.sel[sl], self.block_table, self.phys[sl],
+                             self.miss_page[sl], self.miss_slot[sl], self.n_miss[sl],
+                             self.status, self.ws)
+        else:
+            ssa_ensure_resident(c, layer0, n_layers, self.sel[sl], self.block_table,
+                                self.miss_page[sl], self.miss_slot[sl], self.n_miss[sl],
+                                self.status, self.ws)
+            ssa_remap_block_table(c, layer0, n_layers, self.sel[sl], self.block_table,
+                                  self.phys[sl], self.status)
         ssa_sparse_paged_decode(c, layer0, n_layers, q, self.sel[sl], self.phys[sl],
                                 self.seq_lens, self.sm_scale, self.out[sl], self.status, self.ws)
 
+    def _preload_step(self, q):
+        L, c = self.layout.n_layers, self.cache
+        scores = self.scores if self.n_steps % 2 == 0 else self.scores_alt
+        main = torch.cuda.current_stream()
+        ssa_index_topk(c, 0, L, q, self.block_table, self.seq_lens, self.sel, self.n_sel, scores,
+                       self.status, self.ws)
+        main.wait_event(self.ev_preload)          # the previous step's preload is done
+        ssa_ensure_remap(c, 0, L, self.sel, self.block_table, self.phys, self.miss_page,
+                         self.miss_slot, self.n_miss, self.status, self.ws)
+        self.ev_remap.record(main)
+        ssa_sparse_paged_decode(c, 0, L, q, self.sel, self.phys, self.seq_lens, self.sm_scale,
+                                self.out, self.status, self.ws)
+        self.side.wait_event(self.ev_remap)
+        ssa_prefetch_pages(c, 0, L, scores, self.block_table, self.seq_lens, self.preload_width,
+                           self.fetch_page, self.fetch_slot, self.n_fetch, self.status, self.ws,
+                           stream=self.side)
+        self.ev_preload.record(self.side)
+        self.last_scores = scores
+        self.n_steps += 1
+
     def step(self, q, per_layer: bool = False, keep_scores: bool = False):
-        """q: bf16 [n_layers][B][Hq][D] on the device, all layers of the cache."""
+        """q: bf16 [n_layers][B][Hq][D] on the device, all layers of the cache.
+        Layer-batched steps take the ensure and the remap in one call
+        (ssa_ensure_remap); per-layer steps make the four separate calls."""
         L = self.layout.n_layers
-        if per_layer:
+        if self.preload_width and not per_layer:
+            self._preload_step(q)
+        elif per_layer:
             for l in range(L):
-                self._calls(q[l:l + 1], l, 1, keep_scores)
+                self._calls(q[l:l + 1], l, 1, keep_scores, fused=False)
         else:
-            self._calls(q, 0, L, keep_scores)
+            self._calls(q, 0, L, keep_scores, fused=True)
         return self.out

@@ -24,13 +24,14 @@ def oracle_state(w: wl.Workload, layers=None) -> oracle.OracleKV:
     return oracle.OracleKV(lay, host_tier=w.host_tier, identity=not w.host_tier)
 
 
-def gpu_runner(w: wl.Workload):
+def gpu_runner(w: wl.Workload, preload_width: int = 0):
     from sparse_attention_decode_indexer_gb300 import Layout
     from sparse_attention_decode_indexer_gb300.runner import DecodeRunner
     lay = Layout(w.page_size, w.n_q_heads, w.n_kv_heads, w.head_dim, w.fp8, w.n_layers,
                  w.logical_pages, w.slots, w.batch, w.pages_per_request, w.block_topk)
     return DecodeRunner(lay, host_tier=w.host_tier, identity=not w.host_tier,
-                        block_table=wl.block_table(w), seq_lens=w.lens)
+                        block_table=wl.block_table(w), seq_lens=w.lens,
+                        preload_width=preload_width)
 
 
 def _u16_to_bf16(a: np.ndarray) -> torch.Tensor:
@@ -105,7 +106,8 @@ def compare_mirror(w, run, orc, l):
 
 
 def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
-               check_pool=True, check_mirror=True, report=None, pool_every_step=True):
+               check_pool=True, check_mirror=True, report=None, pool_every_step=True,
+               preload_width=0):
     """Run ``steps`` decode steps of ``w`` on both sides and compare.
 
     The library always runs every layer (one launch per stage covers them
@@ -115,7 +117,7 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
     oracle_layers = list(range(w.n_layers)) if oracle_layers is None else list(oracle_layers)
     steps = w.steps if steps is None else steps
     orc = oracle_state(w)
-    run = gpu_runner(w)
+    run = gpu_runner(w, preload_width)
     prefill(w, run, orc, oracle_layers)
     assert int(run.status.item()) == 0, f"status {run.status.item()}"
     for l in oracle_layers:
@@ -128,6 +130,7 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
     max_err = 0.0
     misses = 0
     max_layer_misses = 0
+    fetched = 0
     for t in range(steps):
         q = np.stack([qs[l][t] for l in range(w.n_layers)])
         qd = _u16_to_bf16(q).cuda()
@@ -137,7 +140,7 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
         for l in oracle_layers:
             r = orc.step(l, qs[l][t], bt, w.lens)
             assert r["drops"] == 0 and r["flags"] == 0 and r["unresolved"] == 0
-            g_scores = run.scores[l].cpu().numpy()
+            g_scores = (run.last_scores if preload_width else run.scores)[l].cpu().numpy()
             assert np.array_equal(g_scores, r["scores"]), f"scores layer {l} step {t}"
             assert np.array_equal(run.sel[l].cpu().numpy(), r["sel"]), f"sel layer {l} step {t}"
             assert np.array_equal(run.n_sel[l].cpu().numpy(), r["n_sel"]), "n_sel"
@@ -146,6 +149,15 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
             assert np.array_equal(run.miss_page[l].cpu().numpy(), r["miss_page"]), "miss_page"
             assert np.array_equal(run.miss_slot[l].cpu().numpy(), r["miss_slot"]), "miss_slot"
             assert np.array_equal(run.phys[l].cpu().numpy(), r["phys"]), f"phys layer {l} step {t}"
+            if preload_width:
+                g_sc = run.last_scores[l].cpu().numpy()
+                assert np.array_equal(g_sc, r["scores"]), f"preload scores layer {l} step {t}"
+                fp, fs, fn, ffl = orc.prefetch(l, preload_width, r["scores"], w.lens, bt)
+                assert ffl == 0
+                assert int(run.n_fetch[l].item()) == fn, f"n_fetch layer {l} step {t}"
+                assert np.array_equal(run.fetch_page[l].cpu().numpy(), fp), "fetch_page"
+                assert np.array_equal(run.fetch_slot[l].cpu().numpy(), fs), "fetch_slot"
+                fetched += fn
             compare_state(w, run, orc, l,
                           check_pool and (pool_every_step or t == steps - 1))
             out = run.out[l].float().cpu().numpy()
@@ -155,5 +167,6 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
             misses += nm
             max_layer_misses = max(max_layer_misses, nm)
     if report is not None:
-        report.update(max_err=max_err, misses=misses, max_layer_misses=max_layer_misses)
+        report.update(max_err=max_err, misses=misses, max_layer_misses=max_layer_misses,
+                      fetched=fetched)
     return run, orc

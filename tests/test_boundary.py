@@ -96,6 +96,7 @@ def test_status_strings(L):
     assert "pool_slots" in L.status_str(-2)
     assert L.status_str(1 | 8) == "drop|unresolved"
     assert L.status_str(32) == "timeout"
+    assert L.status_str(64 | 2) == "bad_id|internal"
 
 
 def test_binding_refuses_to_run_without_the_library(tmp_path, monkeypatch):

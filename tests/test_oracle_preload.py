@@ -180,3 +180,20 @@ def test_random_traces_match_an_independent_model(fp8):
             assert np.array_equal(kv.v_pool[0, s], kv.v_mirror[0, po[s]])
         # with S >= B*W every candidate fits
         assert all(so[i] >= 0 for i in cand_ids)
+
+
+def test_attention_from_the_mirror_equals_attention_from_the_pool():
+    # the mirror holds the pool's bytes, so once the selection is resident the
+    # attention read from the mirror (logical ids as slots) is the same, bit
+    # for bit, as the one read from the pool through the remapped table
+    w, kv = _kv(B=2, n=40, S=2 * 20, k=5, fp8=True)
+    bt, lens = block_table(w), w.lens
+    from workloads import queries
+    q = queries(w.with_(steps=1), 0)[0]
+    sel, n_sel, scores, _, _ = kv.index_topk(0, q, bt, lens)
+    kv.ensure(0, sel, bt)
+    phys, unresolved = kv.remap(0, sel, bt)
+    assert unresolved == 0
+    a = kv.decode(0, q, sel, phys, lens)
+    b = kv.decode_from_mirror(0, q, sel, bt, lens)
+    assert np.array_equal(a, b)

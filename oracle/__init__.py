@@ -79,6 +79,8 @@ def _load():
         lib.or_remap.argtypes = [vp] * 5
         lib.or_decode.restype = None
         lib.or_decode.argtypes = [vp] * 9 + [ctypes.c_double, vp]
+        lib.or_ensure_shared.restype = i32
+        lib.or_ensure_shared.argtypes = [vp, i32] + [vp] * 17
         lib.or_prefetch.restype = i32
         lib.or_prefetch.argtypes = [vp, i32] + [vp] * 18
         lib.or_set_threads.restype = None
@@ -228,6 +230,39 @@ class OracleKV:
             _p(self._mir(self.v_scale_m, l)), _p(self.k_pool[l]), _p(self.v_pool[l]),
             _p(self.k_scale[l]), _p(self.v_scale[l]), _p(mp), _p(ms), _p(nm))
         return mp, ms, int(nm[0]), flags
+
+    # -- NEXT-2: one residency for a layer range ----------------------------
+    def ensure_shared(self, layer0: int, n_layers: int, sel: np.ndarray, bt: np.ndarray):
+        """Ensure the union of the layers' selections (sel [n][B][W]) on the
+        first layer's LRU state; every miss copied for every layer of the
+        range (or_ensure_shared)."""
+        lib, lay = _load(), self.lay.c()
+        n = n_layers
+        l0, l1 = layer0, layer0 + n
+        BW = self.lay.batch * self.lay.max_sel
+        mp = np.empty((n * BW,), np.int32)
+        ms = np.empty((n * BW,), np.int32)
+        nm = np.zeros((1,), np.int32)
+        mir = self.k_mirror is not None
+        flags = lib.or_ensure_shared(
+            ctypes.byref(lay), n, _p(self.slot_of[l0]), _p(self.page_of[l0]),
+            _p(self.last_use[l0]), _p(self.clock[l0:l0 + 1]), _p(np.ascontiguousarray(sel, np.int32)),
+            _p(np.ascontiguousarray(bt, np.int32)),
+            _p(self.k_mirror[l0:l1] if mir else None), _p(self.v_mirror[l0:l1] if mir else None),
+            _p(self.k_scale_m[l0:l1] if mir else None), _p(self.v_scale_m[l0:l1] if mir else None),
+            _p(self.k_pool[l0:l1]), _p(self.v_pool[l0:l1]), _p(self.k_scale[l0:l1]),
+            _p(self.v_scale[l0:l1]), _p(mp), _p(ms), _p(nm))
+        return mp, ms, int(nm[0]), flags
+
+    def remap_shared(self, layer0: int, layer: int, sel: np.ndarray, bt: np.ndarray):
+        """Remap of one layer's selection through the shared state (the first
+        layer's slot_of)."""
+        lib, lay = _load(), self.lay.c()
+        phys = np.empty((self.lay.batch, self.lay.max_sel), np.int32)
+        unresolved = lib.or_remap(ctypes.byref(lay), _p(self.slot_of[layer0]),
+                                  _p(np.ascontiguousarray(sel, np.int32)),
+                                  _p(np.ascontiguousarray(bt, np.int32)), _p(phys))
+        return phys, unresolved
 
     # -- NEXT-1: top-k preload ----------------------------------------------
     def prefetch(self, layer: int, width: int, scores: np.ndarray, seq_lens: np.ndarray,

@@ -473,6 +473,61 @@ int or_ensure(const or_layout *L, int32_t *slot_of, int32_t *page_of,
 }
 
 /* ------------------------------------------------------------------------ */
+/* NEXT-2: residency shared by the layers of a call                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [FT499] "Design", residency engine bullet: one launch copies a page's K and
+ * V for all the sparse-attention layers, i.e. a logical page is resident (or
+ * not) for every layer at once.  Reading: for a call over layers
+ * [0, n_layers) (the arrays below are those layers' consecutive slices), one
+ * LRU state -- the first layer's slot_of / page_of / last_use / clock -- is
+ * shared; the ensure works on the union of every layer's selection with the
+ * order of events of or_ensure (distinct ids ascending, hits touched, misses
+ * ascending take victims, clock + 1), and each miss is copied mirror -> slot
+ * for every layer.  The other layers' LRU arrays are not used.  The state
+ * update is exactly or_ensure on the layers' selections stacked as one batch
+ * of n_layers * B requests; the copy then repeats for layers 1..n-1.
+ *   sel [n_layers][B][W]; pools and mirrors: [n_layers] slices of the
+ *   per-layer layouts; miss lists [n_layers * B * W].
+ */
+int or_ensure_shared(const or_layout *L, int n_layers, int32_t *slot_of, int32_t *page_of,
+                     int32_t *last_use, int32_t *clock, const int32_t *sel, const int32_t *bt,
+                     const uint8_t *k_mirror, const uint8_t *v_mirror,
+                     const float *k_scale_m, const float *v_scale_m,
+                     uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float *v_scale,
+                     int32_t *miss_page, int32_t *miss_slot, int32_t *n_miss) {
+  or_layout Lu = *L;
+  Lu.B = L->B * n_layers;
+  int32_t *btu = (int32_t *)malloc(sizeof(int32_t) * (size_t)Lu.B * L->n_max);
+  for (int l = 0; l < n_layers; ++l)
+    memcpy(btu + (size_t)l * L->B * L->n_max, bt, sizeof(int32_t) * (size_t)L->B * L->n_max);
+  const size_t esz = L->fp8 ? 1 : 2;
+  const size_t pbytes = page_elems(L) * esz;
+  const size_t mirror_layer = (size_t)L->Lp * pbytes, pool_layer = (size_t)L->S * pbytes;
+  int flags = or_ensure(&Lu, slot_of, page_of, last_use, clock, sel, btu,
+                        k_mirror, v_mirror, k_scale_m, v_scale_m,
+                        k_pool, v_pool, k_scale, v_scale, miss_page, miss_slot, n_miss);
+  for (int l = 1; l < n_layers; ++l)
+    for (int i = 0; i < *n_miss; ++i) {
+      const int id = miss_page[i], v = miss_slot[i];
+      if (!(k_mirror && v_mirror)) continue;
+      memcpy(k_pool + l * pool_layer + (size_t)v * pbytes,
+             k_mirror + l * mirror_layer + (size_t)id * pbytes, pbytes);
+      memcpy(v_pool + l * pool_layer + (size_t)v * pbytes,
+             v_mirror + l * mirror_layer + (size_t)id * pbytes, pbytes);
+      if (L->fp8) {
+        memcpy(k_scale + ((size_t)l * L->S + v) * L->P, k_scale_m + ((size_t)l * L->Lp + id) * L->P,
+               sizeof(float) * L->P);
+        memcpy(v_scale + ((size_t)l * L->S + v) * L->P, v_scale_m + ((size_t)l * L->Lp + id) * L->P,
+               sizeof(float) * L->P);
+      }
+    }
+  free(btu);
+  return flags;
+}
+
+/* ------------------------------------------------------------------------ */
 /* NEXT-1: top-k preload                                                      */
 /* ------------------------------------------------------------------------ */
 

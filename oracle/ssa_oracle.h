@@ -86,6 +86,16 @@ void or_decode(const or_layout *L, const uint8_t *k_pool, const uint8_t *v_pool,
                const int32_t *sel, const int32_t *phys, const int32_t *seq_lens,
                double sm_scale, double *out);
 
+/* --- NEXT-2: one residency for the layers of a call -------------------- */
+/* State: the first layer's arrays; sel [n_layers][B][W]; pools, scales and
+ * mirrors: n_layers consecutive per-layer slices; miss lists [n_layers*B*W]. */
+int or_ensure_shared(const or_layout *L, int n_layers, int32_t *slot_of, int32_t *page_of,
+                     int32_t *last_use, int32_t *clock, const int32_t *sel, const int32_t *bt,
+                     const uint8_t *k_mirror, const uint8_t *v_mirror,
+                     const float *k_scale_m, const float *v_scale_m,
+                     uint8_t *k_pool, uint8_t *v_pool, float *k_scale, float *v_scale,
+                     int32_t *miss_page, int32_t *miss_slot, int32_t *n_miss);
+
 /* --- NEXT-1: top-k preload after a step's ensure ---------------------- */
 /* scores: [B][n_max] of the step (or_index_scores); 1 <= width <= W (else
  * -1).  miss lists [B*W] (-1 after n_miss).  Returns flags as or_ensure. */

@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-legs", action="store_true",
+                    help="skip the preload, host-tail, shared-residency and store legs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bound on the timed oracle sample")
@@ -418,7 +420,7 @@ def run_ours(args, rank: int, world: int, dist):
     W, K = args.warmup, args.steps
     H_max = args.host_warmup if args.host_warmup >= 0 else (300 if w.host_tier else 0)
     run = build_runner(w, rank, prefill_now=False)   # graphs first, then one prefill
-    n_total = H_max + W + 4 * K + (6 * K + 16 if w.host_tier else 0)
+    n_total = H_max + W + 4 * K + (8 * K + 100 if w.host_tier else 0)
     q_all = queries_all(w, n_total)
     q_cur = q_all[0].clone()
     flush_w = torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB > L2
@@ -627,12 +629,14 @@ def run_ours(args, rank: int, world: int, dist):
                "path": "DecodeRunner.step (4 C-ABI calls, direct launches) + pinned H2D q / D2H out"}
 
     preload = host_tail = None
-    if w.host_tier:
+    if w.host_tier and not args.no_legs:
         preload = time_preload(w, run, q_all, H + W + 4 * K, K, flush_l2)
         host_tail = time_host_tail(w, run, q_all, H + W + 8 * K + 8, K, flush_l2)
     if rank != 0:
         return None
-    store = time_store(w, run)
+    shared = (time_shared(w, run, q_all, H + W + 10 * K + 16, K, flush_l2)
+              if w.host_tier and not args.no_legs else None)
+    store = time_store(w, run) if not args.no_legs else None
     peak, peak_kind = load_peaks()
     dec_ms = statistics.mean(stage_ms["decode"])
     dec_bytes = decode_bytes(w)
@@ -697,11 +701,14 @@ def run_ours(args, rank: int, world: int, dist):
     }
     if e2e is not None:
         line["e2e"] = e2e
-    line["store"] = store
+    if store is not None:
+        line["store"] = store
     if preload is not None:
         line["preload"] = preload
     if host_tail is not None:
         line["host_tail"] = host_tail
+    if shared is not None:
+        line["shared_residency"] = shared
     return line, w
 
 
@@ -813,6 +820,54 @@ def time_host_tail(w: wl.Workload, run, q_all, t0: int, K: int, flush_l2):
     st = int(run.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st} in the host-tail leg")
+    return out
+
+
+def time_shared(w: wl.Workload, run, q_all, t0: int, K: int, flush_l2, warm: int = 40):
+    """Residency shared by all layers (ssa_ensure_remap_shared: one LRU, each
+    miss copied for every layer) against per-layer residency, both eager
+    DecodeRunner steps with an L2 flush before each.  The residency state is
+    emptied first and each mode warmed for `warm` steps (the first fetches
+    after an empty pool run far slower over the host link).  Run last: it
+    leaves the cache in shared mode."""
+    import torch
+    L, B, W, S = w.n_layers, w.batch, 2 * w.block_topk + 8, w.slots
+    if L * B * W > 16384 or S < min(L * B * W, w.logical_pages):
+        return {"not_applicable": f"pool of {S} slots < {L} layers x {B * W} selection "
+                                  f"entries (the union the shared state must hold)"}
+    c = run.cache
+    out = {}
+    t = t0
+    for name, shared in (("per_layer", False), ("shared", True)):
+        torch.cuda.synchronize()
+        for a, v in ((c.slot_of, -1), (c.page_of, -1), (c.last_use, -1), (c.clock, 0)):
+            a.fill_(v)                             # an empty pool for each mode
+        run.shared_residency = shared
+        for _ in range(warm):
+            flush_l2()
+            run.step(q_all[t]); t += 1
+        torch.cuda.synchronize()
+        ms, miss = [], 0
+        for _ in range(K):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run.step(q_all[t]); t += 1
+            e1.record()
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+            miss += int(run.n_miss[0].item()) if shared else int(run.n_miss.sum().item())
+        per_miss = page_fetch_bytes(w) * (L if shared else 1)
+        out[name] = {"ms_per_step": statistics.mean(ms),
+                     "value": L * B / (statistics.mean(ms) * 1e-3),
+                     "misses_per_step": miss / K,
+                     "miss_bytes_per_step": miss / K * per_miss}
+    out["ratio"] = out["shared"]["ms_per_step"] / out["per_layer"]["ms_per_step"]
+    out["note"] = ("eager DecodeRunner.step after an emptied pool and %d warm steps per mode; "
+                   "a shared miss copies the page for every layer" % warm)
+    st = int(run.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the shared-residency leg")
     return out
 
 

@@ -254,6 +254,30 @@ int ssa_ensure_remap(const ssa_layout *lay, const ssa_cache *c, int layer0, int 
                      int32_t *status, void *ws, ssa_stream_t stream);
 
 /*
+ * Residency shared by the layers of a call (FreeToken PR #499, "Design": one
+ * launch copies a page's K and V for all the sparse-attention layers).  The
+ * layers [layer0, layer0 + n_layers) share ONE LRU state, layer0's slot_of /
+ * page_of / last_use / clock (the other layers' state arrays are not used):
+ *   1. U = distinct logical ids selected by any layer of the range, ascending;
+ *   2-5. as ssa_ensure_resident, on that one state: hits touched, misses take
+ *      free slots then untouched slots by (last_use, slot), rebind, clock + 1;
+ *      each miss's K, V (and fp8 scales) are copied into the same slot of
+ *      EVERY layer's pool (one launch for all layers);
+ *   then phys [n_layers][B][W] = slot_of[layer0][bt[b][sel]] for every layer.
+ *   miss_page_opt, miss_slot_opt [n_layers * B * W] int32 out or NULL
+ *   n_miss_opt  [1] int32 out or NULL: misses of the call
+ * Requires n_layers * B * W <= 16384 (SSA_ERR_UNSUPPORTED) and pool_slots >=
+ * min(n_layers * B * W, logical_pages) (SSA_ERR_POOL_TOO_SMALL).  Use one
+ * residency mode per cache: this call and ssa_ensure_resident / ssa_ensure_remap
+ * keep different state.
+ */
+int ssa_ensure_remap_shared(const ssa_layout *lay, const ssa_cache *c, int layer0,
+                            int n_layers, const int32_t *sel, const int32_t *block_table,
+                            int32_t *phys, int32_t *miss_page_opt, int32_t *miss_slot_opt,
+                            int32_t *n_miss_opt, int32_t *status, void *ws,
+                            ssa_stream_t stream);
+
+/*
  * Top-k preload (vLLM RFC #33980, "Motivation" point 2 and "Proposed Change":
  * "Topk KV preload" -- adjacent decode steps select largely the same pages,
  * so a former top-k can drive a fetch that overlaps the current step's

@@ -35,7 +35,8 @@ EXPORTS = ("ssa_workspace_size", "ssa_lru_init", "ssa_store_kv_mirror", "ssa_ind
            "ssa_ensure_resident", "ssa_remap_block_table", "ssa_sparse_paged_decode",
            "ssa_status_str", "ssa_last_cuda_error", "ssa_launch_count",
            "ssa_index_topk_static_scratch", "ssa_selftest_bounded_wait", "ssa_host_read_probe",
-           "ssa_prefetch_pages", "ssa_ensure_remap", "ssa_sparse_paged_decode_host_tail")
+           "ssa_prefetch_pages", "ssa_ensure_remap", "ssa_sparse_paged_decode_host_tail",
+           "ssa_ensure_remap_shared")
 
 
 class SsaError(RuntimeError):
@@ -96,6 +97,8 @@ def lib():
         L.ssa_sparse_paged_decode_host_tail.argtypes = ([P(SsaLayout), P(SsaCache), i32, i32, vp,
                                                          vp, vp, vp, ctypes.c_float, vp, vp, vp,
                                                          vp])
+        L.ssa_ensure_remap_shared.restype = i32
+        L.ssa_ensure_remap_shared.argtypes = [P(SsaLayout), P(SsaCache), i32, i32] + [vp] * 9
         L.ssa_ensure_remap.restype = i32
         L.ssa_ensure_remap.argtypes = [P(SsaLayout), P(SsaCache), i32, i32] + [vp] * 9
         L.ssa_prefetch_pages.restype = i32
@@ -257,6 +260,17 @@ def ssa_ensure_remap(cache: KVCache, layer0: int, n_layers: int, sel, block_tabl
                                   n_layers, _ptr(sel), _ptr(block_table), _ptr(phys),
                                   _ptr(miss_page), _ptr(miss_slot), _ptr(n_miss), _ptr(status),
                                   _ptr(ws), _stream(stream)))
+
+
+def ssa_ensure_remap_shared(cache: KVCache, layer0: int, n_layers: int, sel, block_table, phys,
+                            miss_page, miss_slot, n_miss, status, ws, stream=None):
+    """One residency for the layer range (layer0's state): the union of the
+    layers' selections ensured, each miss copied for every layer, phys for
+    every layer."""
+    _check(lib().ssa_ensure_remap_shared(ctypes.byref(cache._lay), ctypes.byref(cache.c), layer0,
+                                         n_layers, _ptr(sel), _ptr(block_table), _ptr(phys),
+                                         _ptr(miss_page), _ptr(miss_slot), _ptr(n_miss),
+                                         _ptr(status), _ptr(ws), _stream(stream)))
 
 
 def ssa_prefetch_pages(cache: KVCache, layer0: int, n_layers: int, scores, block_table,

@@ -256,6 +256,34 @@ int ssa_ensure_remap(const ssa_layout* lay, const ssa_cache* c, int layer0, int 
                      n_miss_opt, phys, status, ws, stream);
 }
 
+int ssa_ensure_remap_shared(const ssa_layout* lay, const ssa_cache* c, int layer0,
+                            int n_layers, const int32_t* sel, const int32_t* block_table,
+                            int32_t* phys, int32_t* miss_page_opt, int32_t* miss_slot_opt,
+                            int32_t* n_miss_opt, int32_t* status, void* ws,
+                            ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if ((r = check_cache(d, c))) return r;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (!sel || !block_table || !phys) return SSA_ERR_INVALID_ARG;
+  if (!ws && (!miss_page_opt || !miss_slot_opt || !n_miss_opt)) return SSA_ERR_INVALID_ARG;
+  const long long entries = (long long)n_layers * d.B * d.W;
+  if (entries > 16384) return SSA_ERR_UNSUPPORTED;      // the union is sorted in shared memory
+  const long long need = entries < d.Lp ? entries : d.Lp;
+  if (d.S < need) return SSA_ERR_POOL_TOO_SMALL;
+  const WsLayout w = ws_layout(d);
+  int32_t* mp = miss_page_opt ? miss_page_opt : at<int32_t>(ws, w.miss_page);
+  int32_t* ms = miss_slot_opt ? miss_slot_opt : at<int32_t>(ws, w.miss_slot);
+  int32_t* nm = n_miss_opt ? n_miss_opt : at<int32_t>(ws, w.n_miss);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_ensure_state_shared(d, *c, layer0, n_layers, sel, block_table, mp, ms,
+                                             nm, phys, status, s);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = launch_miss_copy(d, *c, layer0, n_layers, mp, ms, nm, status, s, true);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
 int ssa_prefetch_pages(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
                        const int32_t* scores, const int32_t* block_table, const int32_t* seq_lens,
                        int width, int32_t* fetch_page_opt, int32_t* fetch_slot_opt,

@@ -43,7 +43,15 @@
 //     whole unit becomes its output, a shared unit's piece an (m, l, o)
 //     partial that it publishes (GPU-scope fence, atomic ticket); the last
 //     piece of a unit to arrive merges the unit's partials into the output.
-//     No CTA ever waits for another, no consumer warp for another.
+//     No CTA ever waits for another, no consumer warp for another;
+//   * every stage's descriptor carries its index in the CTA's stream, which
+//     the consumers check against the stage they waited for
+//     (SSA_ST_INTERNAL if it ever differs);
+//   * host-tail mode (ssa_sparse_paged_decode_host_tail): the producer
+//     resolves each selected page through slot_of itself; a page without a
+//     slot is copied from the pinned host mirror by the producer warp's
+//     16-byte cp.async loads over UVA into the same swizzled stage layout,
+//     the stage's barrier tracking those copies instead of a TMA byte count.
 // The work is HBM-bound (8 flop/byte bf16, 16 fp8): the tensor cores carry
 // the G-row tiles, the memory system sets the pace.
 #include <cudaTypedefs.h>
@@ -73,46 +81,34 @@ constexpr int kSmemPerCtaMax = 227 * 1024;
 constexpr int kSmemReservedPerCta = 1024;
 
 // stage descriptor flags
-constexpr int kQ = 1;       // the stage also holds the unit's q rows
-constexpr int kFlush = 2;   // no data: the end of a piece (one such stage per consumer warp)
-constexpr int kDone = 4;    // no data: the end of the CTA's range (one per consumer warp)
-constexpr int kSeqShift = 4;  // the descriptor's flags word holds the chunk index above this
+constexpr int kFirst = 1;   // first page of a piece: the stage also holds q
+constexpr int kLast = 2;    // last page of a piece: flush after it
+constexpr int kEmpty = 4;   // a piece without pages (no data in the stage)
+constexpr int kDone = 8;    // end of the CTA's range
+constexpr int kFinal = 16;  // with kLast / kEmpty: the CTA's last piece
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// A stage holds one chunk: up to kCT tokens of one page of one KV head (K and
-// V tiles, fp8 scales) and, for a consumer warp's first chunk of a unit, the
-// unit's q rows.  One consumer warp processes a whole chunk (kNB 16-token
-// blocks, their MMA chains interleaved); chunk j of the CTA's stream goes to
-// consumer warp j % 4 and stage j % kStages (a multiple of 4, so each stage
-// serves one warp).
 template <bool FP8, int P>
 struct Cfg {
-  static constexpr int kCT = FP8 ? (P < 64 ? P : 64) : (P < 32 ? P : 32);   // tokens per chunk
-  static constexpr int kChunks = P / kCT;                                     // chunks per page
-  static constexpr int kNB = kCT / 16;                                        // blocks per chunk
-  static constexpr int kTileBytes = kCT * kD * (FP8 ? 1 : 2);    // K (or V) of one chunk
-  static constexpr int kScaleBytes = FP8 ? 2 * kCT * 4 : 0;
+  static constexpr int kTileBytes = P * kD * (FP8 ? 1 : 2);      // one KV head of one page
+  static constexpr int kScaleBytes = FP8 ? 2 * P * 4 : 0;
   static constexpr int kQOff = 2 * kTileBytes + kScaleBytes;
   static constexpr int kQBytes = kMaxG * kD * 2;
   static constexpr int kStageBytes = round_up(kQOff + kQBytes, 1024);
   static constexpr int kCombineBytes = kConsumerWarps * kMaxG * kD * 4 + 2 * kConsumerWarps * kMaxG * 4;
   // alignment slack, combine area, producer window, descriptors and barriers
   static constexpr int kFixed = 1024 + kCombineBytes + kWindow * 8 + kMaxStages * 32 + 64;
-  // two CTAs per SM when at least four stages fit beside the second CTA
+  // two CTAs per SM when at least two stages fit beside the second CTA
   static constexpr int kStages2 = (kSmemPerSm / 2 - kSmemReservedPerCta - kFixed) / kStageBytes;
-  static constexpr int kCtasPerSm = kStages2 >= 4 ? 2 : 1;
+  static constexpr int kCtasPerSm = kStages2 >= 2 ? 2 : 1;
   static constexpr int kStagesFit =
       kCtasPerSm == 2 ? kStages2 : (kSmemPerCtaMax - kFixed) / kStageBytes;
-  // a multiple of the consumer warps: chunk j takes stage j % kStages and goes
-  // to warp j % 4, so every stage belongs to one warp, and a warp's wait on a
-  // stage's barrier parity always follows its own wait on the previous phase
-  static constexpr int kStages =
-      (kStagesFit > kMaxStages ? kMaxStages : kStagesFit) / kConsumerWarps * kConsumerWarps;
-  // log2 of the fp8 V^T row swizzle span in 16-byte units (row = kCT bytes)
-  static constexpr int kVSwz = kCT >= 128 ? 3 : (kCT == 64 ? 2 : (kCT == 32 ? 1 : 0));
-  static_assert(kStages >= kConsumerWarps && kStages % kConsumerWarps == 0,
-                "whole stages per consumer warp");
+  static constexpr int kStages = kStagesFit > kMaxStages ? kMaxStages : kStagesFit;
+  static constexpr int kBlocks = P / 16;                          // 16-token blocks per page
+  // log2 of the fp8 V^T row swizzle span in 16-byte units (row = P bytes)
+  static constexpr int kVSwz = P >= 128 ? 3 : (P == 64 ? 2 : (P == 32 ? 1 : 0));
+  static_assert(kStages >= 2, "at least two stages");
   static_assert(kQOff % 16 == 0, "q rows need a 16-byte aligned bulk copy");
 };
 
@@ -186,6 +182,24 @@ __device__ __forceinline__ float bf16x8_absmax(uint4 v) {
   return m;
 }
 
+// The merge of a unit's pieces (a7), written once so that the merge warp and
+// the consumer warps, whichever holds the unit's last piece to finish, do
+// the same arithmetic in the same order and the output does not depend on
+// which piece arrives last: per (head, 4 columns) an online max / sum /
+// weighted sum over the pieces in piece order.
+__device__ __forceinline__ void merge_online(float& M, float& L, float4& acc, float2 ml,
+                                             float4 x) {
+  if (ml.x == -INFINITY) return;                // a piece with no token of this unit
+  const float mn = fmaxf(M, ml.x);
+  const float a = fast_exp2(M - mn), b = fast_exp2(ml.x - mn);
+  L = fmaf(ml.y, b, L * a);
+  acc.x = fmaf(x.x, b, acc.x * a);
+  acc.y = fmaf(x.y, b, acc.y * a);
+  acc.z = fmaf(x.z, b, acc.z * a);
+  acc.w = fmaf(x.w, b, acc.w * a);
+  M = mn;
+}
+
 // First tile of CTA c (the first tr CTAs hold tq + 1 tiles, the others
 // tq), and the CTA that holds tile t (the inverse).
 __device__ __forceinline__ int tile_begin(const DecodeParams& p, int c) {
@@ -196,7 +210,10 @@ __device__ __forceinline__ int cta_of(const DecodeParams& p, int t) {
   return t < big ? t / (p.tq + 1) : p.tr + (t - big) / p.tq;
 }
 
-template <bool FP8, int P>
+// HT: host-tail mode (pages resolved through slot_of; pages without a slot
+// read from the mirror) -- a separate instantiation, so that the resident
+// path carries none of its code
+template <bool FP8, int P, bool HT>
 __global__ void __launch_bounds__(kDecodeThreads, Cfg<FP8, P>::kCtasPerSm)
 decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV) {
@@ -225,7 +242,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);           // the one consumer warp of the chunk
+      mbar_init(&empty[i], kConsumerWarps);
     }
     mbar_init(cfull, kConsumerWarps);
     mbar_init(cfree, 1);
@@ -326,46 +343,33 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       auto piece = [&](int kk) -> size_t {
         return ((size_t)(c_first + kk) * 2 + (kk == 0 ? slot0 : 0)) * p.G;
       };
-      // lane g < G: running max and sum of head g over the pieces
-      float Mu = -INFINITY, Lu = 0.0f;
-      if (lane < p.G) {
-#pragma unroll 4
-        for (int kk = 0; kk < np; ++kk) {
-          const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + piece(kk) + lane);
-          if (ml.x > Mu) {
-            Lu *= fast_exp2(Mu - ml.x);
-            Mu = ml.x;
-          }
-          if (ml.x != -INFINITY) Lu += ml.y * fast_exp2(ml.x - Mu);
-        }
-      }
-      const float invL = Lu > 0.0f ? 1.0f / Lu : 0.0f;
-      // lane holds d = 4*lane..4*lane+3 of every head; a piece's weight
-      // comes from its head's lane
+      // lane: d = 4*lane..4*lane+3 of every head; pieces in order
+      const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
       const float4* po = reinterpret_cast<const float4*>(p.part_o);
+      float Mh[kMaxG], Lh[kMaxG];
       float4 acc[kMaxG];
 #pragma unroll
-      for (int jj = 0; jj < kMaxG; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int jj = 0; jj < kMaxG; ++jj) {
+        Mh[jj] = -INFINITY;
+        Lh[jj] = 0.0f;
+        acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       for (int kk = 0; kk < np; ++kk) {      // a piece's vectors per round trip
-        float f = 0.0f;
-        if (lane < p.G && Mu != -INFINITY)
-          f = fast_exp2(__ldcg(&p.part_ml[(piece(kk) + lane) * 2]) - Mu);
+        float2 ml[kMaxG];
         float4 x[kMaxG];
 #pragma unroll
-        for (int jj = 0; jj < kMaxG; ++jj)
+        for (int jj = 0; jj < kMaxG; ++jj) {
+          ml[jj] = jj < p.G ? __ldcg(pml + piece(kk) + jj) : make_float2(-INFINITY, 0.0f);
           x[jj] = jj < p.G ? __ldcg(po + (piece(kk) + jj) * (kD / 4) + lane)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int jj = 0; jj < kMaxG; ++jj) {
-          const float wj = __shfl_sync(0xffffffffu, f, jj);
-          acc[jj].x += wj * x[jj].x; acc[jj].y += wj * x[jj].y;
-          acc[jj].z += wj * x[jj].z; acc[jj].w += wj * x[jj].w;
         }
+#pragma unroll
+        for (int jj = 0; jj < kMaxG; ++jj) merge_online(Mh[jj], Lh[jj], acc[jj], ml[jj], x[jj]);
       }
 #pragma unroll
       for (int jj = 0; jj < kMaxG; ++jj) {
-        const float r = __shfl_sync(0xffffffffu, invL, jj);
         if (jj < p.G) {
+          const float r = Lh[jj] > 0.0f ? 1.0f / Lh[jj] : 0.0f;
           uint2 pk;
           pk.x = pack_bf16(acc[jj].x * r, acc[jj].y * r);
           pk.y = pack_bf16(acc[jj].z * r, acc[jj].w * r);
@@ -379,17 +383,13 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
 
   if (warp == kProducerWarp) {
     // ---------------- producer warp ----------------------------------------
-    // The warp reads and compacts the rows; lane 0 alone issues the copies.
-    // Chunks go out in range order: chunk st to stage st % NST, for consumer
-    // warp st % 4.  The first four chunks of a piece carry the unit's q rows
-    // (they reach four different warps, so every warp that gets any chunk of
-    // the piece gets q with its first one).  After each piece but the CTA's
-    // last come four kFlush stages, one per consumer warp, and after the last
-    // piece four kDone stages: a warp ends its piece on its marker, which
-    // depends on no stage issued later (so no warp waits, holding a stage,
-    // for a flush that needs a stage not yet issued).
-    constexpr int CT = C::kCT;
-    int st = 0;                 // chunks issued (every lane keeps the count)
+    // The warp reads and compacts the rows; lane 0 issues the TMA loads (the
+    // resident path issues pages from lane 0 alone; the host-tail path from
+    // the whole warp, every lane its share of 16-byte copies for a page
+    // without a slot).  Lane 0's st counts the stages.  A stage's descriptor
+    // carries it, and the consumers check it against the stage they waited
+    // for.
+    int st = 0;
     bool ok = true;
     int cur_row = -1, cnt = 0, seq_len = 0;
     int pgc[4], slc[4];        // the row's first 128 entries, kept for the second pass
@@ -397,93 +397,88 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     auto acquire = [&](int s) -> bool {      // lane 0: stage slot s % NST is free
       return s < NST || mbar_wait(&empty[s % NST], ((s / NST) - 1) & 1, &s_abort);
     };
-    // meta.x: the flags and, above them, the chunk's index in the stream
-    // (the consumer checks it against the index it waited for).  Called by
-    // the whole warp; st advances in every lane.
-    auto issue_marker = [&](int kind, int piece) -> bool {
+    auto acquire_warp = [&]() -> bool {
       bool acq = lane == 0 ? acquire(st) : true;
-      acq = __shfl_sync(0xffffffffu, acq, 0);
-      if (!acq) return false;
+      return __shfl_sync(0xffffffffu, acq, 0);
+    };
+    auto issue_marker = [&](int kind, int unit) -> bool {   // the whole warp
+      if (!acquire_warp()) return false;
       const int sb = st % NST;
       if (lane == 0) {
-        meta[sb] = make_int4(kind | (st << kSeqShift), 0, 0, piece);
+        meta[sb] = make_int4(kind, 0, unit, st);
         mbar_arrive(&full[sb]);
       }
       ++st;
       return true;
     };
 
-    // chunk ci of one page of K and V (one KV head), its fp8 scales and,
-    // with kQ, the unit's q rows.  Resident pages (ent.y >= 0, a slot) come
-    // by TMA from the pool; host-tail pages (ent.y <= -2, logical id
-    // -2 - ent.y) by 16-byte cp.async copies from the pinned mirror, every
-    // lane a share, into the same swizzled stage layout.  Called by the
-    // whole warp.
-    auto issue_chunk = [&](int2 ent, int ci, int flags, int unit, int piece, int h, int layer,
-                           int seq_len) -> bool {
-      bool acq = lane == 0 ? acquire(st) : true;
-      acq = __shfl_sync(0xffffffffu, acq, 0);
-      if (!acq) return false;
+    // one page of K and V (one KV head), its fp8 scales and, on the first
+    // page of a piece, the unit's q rows.  Resident pages (ent.y >= 0, a
+    // slot) come by TMA from the pool; host-tail pages (ent.y <= -2, logical
+    // id -2 - ent.y) by 16-byte cp.async copies from the pinned mirror, every
+    // lane a share, into the same swizzled stage layout.  The whole warp.
+    auto issue_page = [&](int2 ent, int flags, int unit, int h, int layer, int seq_len) -> bool {
+      if (!(HT ? acquire_warp() : acquire(st))) return false;   // resident path: lane 0 alone
       const int sb = st % NST;
       uint8_t* stage = ring + sb * C::kStageBytes;
-      const uint32_t qbytes = (flags & kQ) ? (uint32_t)p.G * kD * 2 : 0u;
-      const bool host = ent.y < 0;
-      if (host) {
+      const uint32_t qbytes = (flags & kFirst) ? (uint32_t)p.G * kD * 2 : 0u;
+      const bool host = HT && ent.y < 0;
+      if constexpr (HT) if (host) {
         const size_t id = (size_t)(-2 - ent.y);
         const size_t pg_bytes = (size_t)p.Hkv * P * kD * (FP8 ? 1 : 2);
         const uint8_t* kpg = p.k_mir + ((size_t)layer * p.Lp + id) * pg_bytes;
         const uint8_t* vpg = p.v_mir + ((size_t)layer * p.Lp + id) * pg_bytes;
         const uint32_t sk = smem_u32(stage), sv = sk + C::kTileBytes;
         if (FP8) {
-          // K rows [CT][128 B] (128-byte swizzle); V d-rows [128][CT B] (kVSwz)
-          for (int i = lane; i < CT * 8; i += 32) {
+          // K rows [P][128 B] (128-byte swizzle); V d-rows [128][P B] (kVSwz)
+          for (int i = lane; i < P * 8; i += 32) {
             const int t = i >> 3, uu = i & 7;
             cp_async16(sk + t * 128 + ((uu ^ (t & 7)) << 4),
-                       kpg + ((size_t)(h * P + ci * CT + t) * 128 + uu * 16));
+                       kpg + ((size_t)(h * P + t) * 128 + uu * 16));
           }
-          constexpr int kVu = CT / 16;                     // 16-byte units per V row
+          constexpr int kVu = P / 16;                      // 16-byte units per V row
           for (int i = lane; i < kD * kVu; i += 32) {
             const int d = i / kVu, uu = i - d * kVu;
-            cp_async16(sv + swz(d * CT + uu * 16, C::kVSwz),
-                       vpg + ((size_t)(h * kD + d) * P + ci * CT + uu * 16));
+            cp_async16(sv + swz(d * P + uu * 16, C::kVSwz),
+                       vpg + ((size_t)(h * kD + d) * P + uu * 16));
           }
-          const size_t so = ((size_t)layer * p.Lp + id) * P + ci * CT;
-          for (int i = lane; i < 2 * (CT / 4); i += 32) {
-            const int which = i / (CT / 4), uu = i - which * (CT / 4);
-            cp_async16(sk + 2 * C::kTileBytes + which * CT * 4 + uu * 16,
+          const size_t so = ((size_t)layer * p.Lp + id) * P;
+          for (int i = lane; i < 2 * (P / 4); i += 32) {
+            const int which = i / (P / 4), uu = i - which * (P / 4);
+            cp_async16(sk + 2 * C::kTileBytes + which * P * 4 + uu * 16,
                        (which ? p.vs_mir : p.ks_mir) + so + uu * 4);
           }
         } else {
-          // K and V rows [CT][256 B] as two 128-byte column halves, swizzled
-          for (int i = lane; i < 2 * CT * 16; i += 32) {
-            const int which = i / (CT * 16), r = i - which * CT * 16;
+          // K and V rows [P][256 B] as two 128-byte column halves, swizzled
+          for (int i = lane; i < 2 * P * 16; i += 32) {
+            const int which = i / (P * 16), r = i - which * P * 16;
             const int t = r >> 4, uu = r & 15, half = uu >> 3, u8 = uu & 7;
-            cp_async16((which ? sv : sk) + half * (CT * 128) + t * 128 + ((u8 ^ (t & 7)) << 4),
-                       (which ? vpg : kpg) + ((size_t)(h * P + ci * CT + t) * 256 + uu * 16));
+            cp_async16((which ? sv : sk) + half * (P * 128) + t * 128 + ((u8 ^ (t & 7)) << 4),
+                       (which ? vpg : kpg) + ((size_t)(h * P + t) * 256 + uu * 16));
           }
         }
         cp_async_mbar_arrive(&full[sb]);
         __syncwarp();                          // every lane's copies are tracked first
       }
       if (lane == 0) {
-        const int nvalid = max(0, min(CT, seq_len - ent.x * P - ci * CT));
-        meta[sb] = make_int4(flags | (st << kSeqShift), nvalid, unit, piece);
+        const int nvalid = max(0, min(P, seq_len - ent.x * P));
+        meta[sb] = make_int4(flags, nvalid, unit, st);
         mbar_arrive_expect_tx(&full[sb],
                               (host ? 0u : (uint32_t)(2 * C::kTileBytes + C::kScaleBytes)) + qbytes);
         if (!host) {
-          const int row_k = ((layer * p.S + ent.y) * p.Hkv + h) * P + ci * CT;
+          const int row_k = ((layer * p.S + ent.y) * p.Hkv + h) * P;
           if (FP8) {
             tma_load_2d(stage, &tmK, &full[sb], 0, row_k);
             const int row_v = ((layer * p.S + ent.y) * p.Hkv + h) * kD;
-            tma_load_2d(stage + C::kTileBytes, &tmV, &full[sb], ci * CT, row_v);
-            const size_t so = ((size_t)layer * p.S + ent.y) * P + ci * CT;
-            bulk_load(stage + 2 * C::kTileBytes, p.k_scale + so, CT * 4, &full[sb]);
-            bulk_load(stage + 2 * C::kTileBytes + CT * 4, p.v_scale + so, CT * 4, &full[sb]);
+            tma_load_2d(stage + C::kTileBytes, &tmV, &full[sb], 0, row_v);
+            const size_t so = ((size_t)layer * p.S + ent.y) * P;
+            bulk_load(stage + 2 * C::kTileBytes, p.k_scale + so, P * 4, &full[sb]);
+            bulk_load(stage + 2 * C::kTileBytes + P * 4, p.v_scale + so, P * 4, &full[sb]);
           } else {
             tma_load_2d(stage, &tmK, &full[sb], 0, row_k);
-            tma_load_2d(stage + CT * 128, &tmK, &full[sb], 64, row_k);
+            tma_load_2d(stage + P * 128, &tmK, &full[sb], 64, row_k);
             tma_load_2d(stage + C::kTileBytes, &tmV, &full[sb], 0, row_k);
-            tma_load_2d(stage + C::kTileBytes + CT * 128, &tmV, &full[sb], 64, row_k);
+            tma_load_2d(stage + C::kTileBytes + P * 128, &tmV, &full[sb], 64, row_k);
           }
         }
         if (qbytes) bulk_load(stage + C::kQOff, p.q + (size_t)unit * p.G * kD, qbytes, &full[sb]);
@@ -499,26 +494,26 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       const int row = u / p.Hkv, h = u - row * p.Hkv;
       const int li = row / p.B, b = row - li * p.B;
       const int layer = p.layer0 + li;
-      const int piece = u - u_first;
       const int32_t* selr = p.sel + (size_t)row * p.W;
-      const int32_t* physr = p.host_tail ? nullptr : p.phys + (size_t)row * p.W;
-      auto physr_or_null = [&](int i) -> int { return physr ? physr[i] : -1; };
+      const int32_t* physr = HT ? nullptr : p.phys + (size_t)row * p.W;
+      auto phys_at = [&](int i) -> int { return physr ? physr[i] : -1; };
       // host tail: the slot of each selected page from slot_of; a page with
-      // no slot is encoded as -2 - (its logical id) and read from the mirror
-      auto resolve = [&](int (&pg)[4], int (&sl)[4], int layer_, int b_) {
+      // no slot is encoded as -2 - (its logical id) and read from the mirror;
+      // an out-of-range id as S (flagged, skipped)
+      auto resolve = [&](int (&pg)[4], int (&sl)[4]) {
         int id[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          id[k] = pg[k] >= 0 && pg[k] < p.nmax ? p.bt[(size_t)b_ * p.nmax + pg[k]] : -1;
+          id[k] = pg[k] >= 0 && pg[k] < p.nmax ? p.bt[(size_t)b * p.nmax + pg[k]] : -1;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const bool ok_id = id[k] >= 0 && id[k] < p.Lp;
-          const int slot = ok_id ? p.slot_of[(size_t)layer_ * p.Lp + id[k]] : -1;
+          const int slot = ok_id ? p.slot_of[(size_t)layer * p.Lp + id[k]] : -1;
           sl[k] = !ok_id ? (pg[k] >= 0 ? p.S : -1) : (slot >= 0 ? slot : -2 - id[k]);
         }
       };
       auto entry_valid = [&](int pg_, int sl_) -> bool {
-        return pg_ >= 0 && ((sl_ >= 0 && sl_ < p.S) || (p.host_tail && sl_ <= -2));
+        return pg_ >= 0 && ((sl_ >= 0 && sl_ < p.S) || (HT && sl_ <= -2));
       };
       if (row != cur_row) {      // count the row's valid entries (once per row)
         cur_row = row;
@@ -530,9 +525,9 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           for (int k = 0; k < 4; ++k) {        // every load of the batch in flight at once
             const int i = base + 32 * k + lane;
             pg[k] = i < p.W ? selr[i] : -1;
-            sl[k] = i < p.W ? physr_or_null(i) : -1;
+            sl[k] = i < p.W ? phys_at(i) : -1;
           }
-          if (p.host_tail) resolve(pg, sl, layer, b);
+          if (HT) resolve(pg, sl);
           if (base == 0) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) { pgc[k] = pg[k]; slc[k] = sl[k]; }
@@ -541,8 +536,8 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const bool valid = entry_valid(pg[k], sl[k]);
-            if (pg[k] >= 0 && sl[k] < 0 && !valid && sl[k] != p.S) bad |= SSA_ST_UNRESOLVED;
             if (pg[k] >= 0 && sl[k] >= p.S) bad |= SSA_ST_BAD_ID;
+            else if (pg[k] >= 0 && !valid) bad |= SSA_ST_UNRESOLVED;
             cnt += __popc(__ballot_sync(0xffffffffu, valid));
           }
           if (bad) set_status(p.status, bad);
@@ -550,16 +545,20 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       }
       // this piece's share [a, e) of the unit's weight, as valid entries [j0, j1)
       const int j0 = (int)((long long)a * cnt / p.w), j1 = (int)((long long)e * cnt / p.w);
-      int seen = j0 == j1 ? p.W : 0, issued = 0;      // no pages: markers only
+      if (j0 == j1) {
+        ok = issue_marker(kEmpty | (u == u_last ? kFinal : 0), u);
+        continue;
+      }
+      int seen = 0, issued = 0;
       for (int base = 0; base < p.W && seen < j1 && ok; base += 4 * 32) {
         int pgv[4], slv[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int i = base + 32 * k + lane;
           pgv[k] = base == 0 ? pgc[k] : (i < p.W ? selr[i] : -1);
-          slv[k] = base == 0 ? slc[k] : (i < p.W ? physr_or_null(i) : -1);
+          slv[k] = base == 0 ? slc[k] : (i < p.W ? phys_at(i) : -1);
         }
-        if (base > 0 && p.host_tail) resolve(pgv, slv, layer, b);
+        if (HT && base > 0) resolve(pgv, slv);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           if (seen >= j1 || !ok) break;
@@ -572,23 +571,20 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           if (in) plist[__popc(mi & lt)] = make_int2(pgv[k], slv[k]);
           __syncwarp();
           const int nw = __popc(mi);
-          for (int x = 0; x < nw && ok; ++x) {
-            const int2 ent = plist[x];
-            for (int ci = 0; ci < C::kChunks && ok; ++ci) {
-              if (ci > 0 && ent.x * P + ci * CT >= seq_len) break;   // past the request's end
-              ok = issue_chunk(ent, ci, issued < kConsumerWarps ? kQ : 0, u, piece, h, layer,
-                               seq_len);
-              ++issued;
+          if (HT || lane == 0) {               // the resident path issues from lane 0 alone
+            for (int x = 0; x < nw && ok; ++x, ++issued) {
+              const int flags = (issued == 0 ? kFirst : 0) |
+                                (issued == j1 - j0 - 1 ? (u == u_last ? kLast | kFinal : kLast) : 0);
+              ok = issue_page(plist[x], flags, u, h, layer, seq_len);
             }
           }
+          if (!HT) ok = __shfl_sync(0xffffffffu, ok, 0);
           __syncwarp();                        // the window is rewritten next round
           seen += __popc(m);
         }
       }
-      if (u < u_last)
-        for (int i = 0; i < kConsumerWarps && ok; ++i) ok = issue_marker(kFlush, piece);
     }
-    for (int i = 0; i < kConsumerWarps && ok; ++i) ok = issue_marker(kDone, u_last - u_first);
+    if (ok) ok = issue_marker(kDone, 0);
     if (lane != 0) return;
     if (!ok) {
       s_abort = 1;
@@ -601,14 +597,9 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   }
 
   // ---------------- consumers -------------------------------------------------
-  // Each consumer warp takes whole chunks (chunk j of the CTA's stream when
-  // j % 4 == warp), the kNB 16-token blocks of a chunk in one pass with their
-  // MMA chains interleaved and one softmax update per chunk.
   // QK^T: A = 16 K rows (tokens), B = q^T (8 heads), C = S^T[token][head].
   // PV:   A = V^T rows (16 of d), B = P^T (C transposed in registers by
   //       movmatrix), C = O^T[d][head].  No MMA row is padding.
-  constexpr int CT = C::kCT;
-  constexpr int NB = C::kNB;
   const int r4 = lane >> 2, c = lane & 3;
 
   uint32_t qb[8][2];
@@ -764,8 +755,9 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     auto piece = [&](int kk) -> size_t {
       return ((size_t)(c_first + kk) * 2 + (kk == 0 ? slot0 : 0)) * p.G;
     };
-    // thread: d = 4*lane..+3 of heads warp and warp + 4; online merge of the
-    // pieces, two pieces' loads per round trip
+    // thread: d = 4*lane..+3 of heads warp and warp + 4; the same merge as
+    // the merge warp's (merge_online in piece order), two pieces' loads per
+    // round trip
     const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
     const float4* po = reinterpret_cast<const float4*>(p.part_o);
     float Mh[2] = {-INFINITY, -INFINITY}, Lh[2] = {0.0f, 0.0f};
@@ -786,18 +778,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float m = ml[kk][hh].x;
-          if (m == -INFINITY) continue;
-          const float mn = fmaxf(Mh[hh], m);
-          const float a = fast_exp2(Mh[hh] - mn), b = fast_exp2(m - mn);
-          Lh[hh] = Lh[hh] * a + ml[kk][hh].y * b;
-          acc[hh].x = acc[hh].x * a + x[kk][hh].x * b;
-          acc[hh].y = acc[hh].y * a + x[kk][hh].y * b;
-          acc[hh].z = acc[hh].z * a + x[kk][hh].z * b;
-          acc[hh].w = acc[hh].w * a + x[kk][hh].w * b;
-          Mh[hh] = mn;
-        }
+        for (int hh = 0; hh < 2; ++hh) merge_online(Mh[hh], Lh[hh], acc[hh], ml[kk][hh], x[kk][hh]);
     }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -814,291 +795,291 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     return true;
   };
 
-  // The chunk stream: a warp ends a piece on its kFlush stage (its state,
-  // possibly empty, goes to the merge warp) and the CTA's last piece on its
-  // kDone stage.
-  bool done = false;
-  for (int j = warp;; j += kConsumerWarps) {
-    const int sb = j % NST;
-    if (!mbar_wait(&full[sb], (j / NST) & 1, &s_abort)) {
-      s_abort = 1;
-      set_status(p.status, SSA_ST_TIMEOUT);
-      break;
-    }
-    const int4 dsc = meta[sb];
-    if ((dsc.x >> kSeqShift) != j) {        // not the chunk this warp waited for
-      s_abort = 1;
-      set_status(p.status, SSA_ST_INTERNAL);
-      break;
-    }
-    if (dsc.x & kDone) {
-      if (lane == 0) mbar_arrive(&empty[sb]);
-      done = true;
-      break;
-    }
-    if (dsc.x & kFlush) {
-      const bool ok = flush();
-      if (lane == 0) mbar_arrive(&empty[sb]);
-      if (!ok) break;
-      continue;
-    }
-    const int nvalid = dsc.y;
-    uint8_t* stage = ring + sb * C::kStageBytes;
-    const uint32_t kb = smem_u32(stage);
-    const uint32_t vb = kb + C::kTileBytes;
-    const float* ksc = reinterpret_cast<const float*>(stage + 2 * C::kTileBytes);
-    const float* vsc = ksc + CT;
-
-    if (dsc.x & kQ) {
-      // the unit's G query rows as the B operand (rows >= G are zero).
-      // bf16: b0 = q[r4][k 2c, 2c+1], b1 = q[r4][k 2c+8, 2c+9] per k16 step.
-      // fp8: q * 2^eq as two e4m3 terms hi + lo (the top and the next four
-      // significant bits: their sum is q * 2^eq to within 2^-10, i.e.
-      // ~2^-18 of |q|max), so QK runs as e4m3 MMAs on the raw K codes;
-      // per k32 step b0 = d 32ks + 4c..+3, b1 = d + 16; qb[ks] = hi,
-      // qb[4 + ks] = lo
-      const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(stage + C::kQOff);
-      const bool row_ok = r4 < p.G;
-      if (FP8) {
-        float amax = 0.0f;
-        for (int i = lane; i < p.G * (kD / 8); i += 32)
-          amax = fmaxf(amax, bf16x8_absmax(*reinterpret_cast<const uint4*>(qs + i * 8)));
-        amax = warp_max(amax);
-        int eq = 0;
-        if (amax > 0.0f) {
-          const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);   // amax in [2^(ef-127), 2^(ef-126))
-          eq = 134 - ef;                                                // amax * 2^eq in [128, 256)
-          eq = eq > 126 ? 126 : (eq < -126 ? -126 : eq);
-        }
-        const float up = exp2f((float)eq);
-        qscale_log2 = p.sm_log2 * exp2f((float)-eq);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const __nv_bfloat16* r = qs + r4 * kD + 32 * ks + 16 * half + 4 * c;
-            float x[4], y[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] = row_ok ? __bfloat162float(r[i]) * up : 0.0f;
-            const uint32_t hi = f32x4_to_e4m3x4(x[0], x[1], x[2], x[3]);
-            e4m3x4_to_f32x4(hi, y[0], y[1], y[2], y[3]);
-            qb[ks][half] = hi;
-            qb[4 + ks][half] = f32x4_to_e4m3x4(x[0] - y[0], x[1] - y[1], x[2] - y[2], x[3] - y[3]);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          qb[ks][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c) : 0u;
-          qb[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c + 8) : 0u;
-        }
-      }
-    }
-
-    // zero V of the tokens past seq_len (their bytes are not ours to trust)
-    if (nvalid < CT) {
-      if (FP8) {
-        for (int i = lane; i < kD * CT; i += 32) {
-          const int d = i / CT, xx = i - d * CT;
-          if (xx >= nvalid) stage[C::kTileBytes + swz(d * CT + xx, C::kVSwz)] = 0;
-        }
-      } else {
-        for (int i = lane; i < CT * 16; i += 32) {
-          const int r = i >> 4, ch = i & 15;
-          if (r >= nvalid)
-            *reinterpret_cast<uint4*>(stage + C::kTileBytes + (ch >> 3) * (CT * 128) + r * 128 +
-                                      (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-    }
-
-    // S^T = K q^T, the chunk's NB blocks side by side; block j rows:
-    // x[j][0], x[j][1] = token 16j + tauA, heads 2c, 2c+1; x[j][2], x[j][3] =
-    // token 16j + tauB
-    float x[NB][4], vsA[NB], vsB[NB];
+  // One call site for each flush, so that its code exists once.
+  int pc = 0;                              // pages processed
+  for (int st = 0;; ++st) {
+    int fkind = 0, funit = u_last;         // 1 = flush, 2 = final_flush
     {
-      // fp8: one accumulator chain per block (the NB blocks give NB
-      // independent chains); bf16: two per block (even and odd k steps)
-      constexpr int NX = FP8 ? 1 : NB;
-      float s4[NB][4], sx[NX][4];
+      const int sb = st % NST;
+      if (!mbar_wait(&full[sb], (st / NST) & 1, &s_abort)) {
+        s_abort = 1;
+        set_status(p.status, SSA_ST_TIMEOUT);
+        break;
+      }
+      const int4 dsc = meta[sb];
+      if (dsc.w != st) {                   // not the stage this warp waited for
+        s_abort = 1;
+        set_status(p.status, SSA_ST_INTERNAL);
+        break;
+      }
+      if (dsc.x & kDone) break;
+      if (dsc.x & kEmpty) {
+        if (lane == 0) mbar_arrive(&empty[sb]);
+        fkind = (dsc.x & kFinal) ? 2 : 1;
+        funit = dsc.z;
+        goto flushes;
+      }
+      const int nvalid = dsc.y;
+      uint8_t* stage = ring + sb * C::kStageBytes;
+      const uint32_t kb = smem_u32(stage);
+      const uint32_t vb = kb + C::kTileBytes;
+      const float* ksc = reinterpret_cast<const float*>(stage + 2 * C::kTileBytes);
+      const float* vsc = ksc + P;
+
+      if (dsc.x & kFirst) {
+        // the unit's G query rows as the B operand (rows >= G are zero).
+        // bf16: b0 = q[r4][k 2c, 2c+1], b1 = q[r4][k 2c+8, 2c+9] per k16 step.
+        // fp8: q * 2^eq as two e4m3 terms hi + lo (the top and the next four
+        // significant bits: their sum is q * 2^eq to within 2^-10, i.e.
+        // ~2^-18 of |q|max), so QK runs as e4m3 MMAs on the raw K codes;
+        // per k32 step b0 = d 32ks + 4c..+3, b1 = d + 16; qb[ks] = hi,
+        // qb[4 + ks] = lo
+        const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(stage + C::kQOff);
+        const bool row_ok = r4 < p.G;
+        if (FP8) {
+          float amax = 0.0f;
+          for (int i = lane; i < p.G * (kD / 8); i += 32)
+            amax = fmaxf(amax, bf16x8_absmax(*reinterpret_cast<const uint4*>(qs + i * 8)));
+          amax = warp_max(amax);
+          int eq = 0;
+          if (amax > 0.0f) {
+            const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);   // amax in [2^(ef-127), 2^(ef-126))
+            eq = 134 - ef;                                                // amax * 2^eq in [128, 256)
+            eq = eq > 126 ? 126 : (eq < -126 ? -126 : eq);
+          }
+          const float up = exp2f((float)eq);
+          qscale_log2 = p.sm_log2 * exp2f((float)-eq);
 #pragma unroll
-      for (int jb = 0; jb < NB; ++jb)
+          for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s4[jb][i] = 0.0f;
+            for (int half = 0; half < 2; ++half) {
+              const __nv_bfloat16* r = qs + r4 * kD + 32 * ks + 16 * half + 4 * c;
+              float x[4], y[4];
 #pragma unroll
-      for (int jb = 0; jb < NX; ++jb)
+              for (int i = 0; i < 4; ++i) x[i] = row_ok ? __bfloat162float(r[i]) * up : 0.0f;
+              const uint32_t hi = f32x4_to_e4m3x4(x[0], x[1], x[2], x[3]);
+              e4m3x4_to_f32x4(hi, y[0], y[1], y[2], y[3]);
+              qb[ks][half] = hi;
+              qb[4 + ks][half] = f32x4_to_e4m3x4(x[0] - y[0], x[1] - y[1], x[2] - y[2], x[3] - y[3]);
+            }
+          }
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sx[jb][i] = 0.0f;
-      if (FP8) {
-        // A = the K codes as they are: a0/a2 = token tkA, d 32ks + 4c..+3 and
-        // d + 16; a1/a3 = token tkB.  The hi and lo terms accumulate in turn.
-        const int xA = tauA & 7, xB = tauB & 7;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-          for (int jb = 0; jb < NB; ++jb) {
-            const uint32_t rA = kb + (16 * jb + tauA) * 128 + 4 * c;
-            const uint32_t rB = kb + (16 * jb + tauB) * 128 + 4 * c;
-            const uint32_t a0 = lds32(rA + (((2 * ks) ^ xA) << 4));
-            const uint32_t a1 = lds32(rB + (((2 * ks) ^ xB) << 4));
-            const uint32_t a2 = lds32(rA + (((2 * ks + 1) ^ xA) << 4));
-            const uint32_t a3 = lds32(rB + (((2 * ks + 1) ^ xB) << 4));
-            mma_e4m3(s4[jb], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-            mma_e4m3(s4[jb], a0, a1, a2, a3, qb[4 + ks][0], qb[4 + ks][1]);
+          for (int ks = 0; ks < 8; ++ks) {
+            qb[ks][0] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c) : 0u;
+            qb[ks][1] = row_ok ? *reinterpret_cast<const uint32_t*>(qs + r4 * kD + 16 * ks + 2 * c + 8) : 0u;
           }
         }
-      } else {
-        const int mi = lane >> 3, rr = lane & 7;
+      }
+
+      // NB 16-token blocks per warp step share one softmax update (max,
+      // rescale, V-scale reference) and interleave their MMA chains.  Two per
+      // step measured no faster than one on GB300 and needs more registers
+      // than two CTAs per SM leave, so one.
+      constexpr int NB = 1;
+      constexpr int kSteps = C::kBlocks / NB;
+#pragma unroll 1
+      for (int bs = 0; bs < kSteps; ++bs) {
+        if (((pc * kSteps + bs) & (kConsumerWarps - 1)) != warp) continue;
+        const int tb0 = bs * NB * 16;
+        // zero V of the tokens past seq_len (their bytes are not ours to trust)
+        if (nvalid < tb0 + NB * 16) {
+          for (int j = 0; j < NB; ++j) {
+            const int tb = tb0 + 16 * j;
+            if (nvalid >= tb + 16) continue;
+            if (FP8) {
+              for (int i = lane; i < kD * 16; i += 32) {
+                const int d = i >> 4, xx = tb + (i & 15);
+                if (xx >= nvalid) stage[C::kTileBytes + swz(d * P + xx, C::kVSwz)] = 0;
+              }
+            } else {
+              for (int i = lane; i < 16 * 16; i += 32) {
+                const int r = tb + (i >> 4), ch = i & 15;
+                if (r >= nvalid)
+                  *reinterpret_cast<uint4*>(stage + C::kTileBytes + (ch >> 3) * (P * 128) +
+                                            r * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+              }
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+
+        // S^T = K q^T per block; rows: x[j][0], x[j][1] = token tkA[j], heads
+        // 2c, 2c+1; x[j][2], x[j][3] = token tkB[j]
+        float x[NB][4], vsA[NB], vsB[NB];
+        int tkA[NB], tkB[NB];
 #pragma unroll
-        for (int ks = 0; ks < 8; ks += 2) {
+        for (int j = 0; j < NB; ++j) {
+          const int tb = tb0 + 16 * j;
+          float s4[4] = {0.f, 0.f, 0.f, 0.f}, sx[4] = {0.f, 0.f, 0.f, 0.f};
+          tkA[j] = tb + tauA;
+          tkB[j] = tb + tauB;
+          if (FP8) {
+            // A = the K codes as they are: a0/a2 = token tkA, d 32ks + 4c..+3
+            // and d + 16; a1/a3 = token tkB.  hi and lo terms in two chains.
+            const uint32_t rA = kb + tkA[j] * 128 + 4 * c, rB = kb + tkB[j] * 128 + 4 * c;
+            const int xA = tkA[j] & 7, xB = tkB[j] & 7;
 #pragma unroll
-          for (int jb = 0; jb < NB; ++jb) {
-            const int t = 16 * jb + (mi & 1) * 8 + rr;
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t a0 = lds32(rA + (((2 * ks) ^ xA) << 4));
+              const uint32_t a1 = lds32(rB + (((2 * ks) ^ xB) << 4));
+              const uint32_t a2 = lds32(rA + (((2 * ks + 1) ^ xA) << 4));
+              const uint32_t a3 = lds32(rB + (((2 * ks + 1) ^ xB) << 4));
+              mma_e4m3(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              mma_e4m3(sx, a0, a1, a2, a3, qb[4 + ks][0], qb[4 + ks][1]);
+            }
+          } else {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int t = tb + (mi & 1) * 8 + rr;
             const uint32_t rowk = kb + t * 128;
             const int xt = t & 7;
-            uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
-            const int c0 = 2 * ks + (mi >> 1), c1 = c0 + 2;     // 16-byte chunks over d
-            ldsm_x4(a0, a1, a2, a3, rowk + (c0 >> 3) * (CT * 128) + (((c0 & 7) ^ xt) << 4));
-            ldsm_x4(a4, a5, a6, a7, rowk + (c1 >> 3) * (CT * 128) + (((c1 & 7) ^ xt) << 4));
-            mma_bf16(s4[jb], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-            mma_bf16(sx[FP8 ? 0 : jb], a4, a5, a6, a7, qb[ks + 1][0], qb[ks + 1][1]);
+#pragma unroll
+            for (int ks = 0; ks < 8; ks += 2) {
+              uint32_t a0, a1, a2, a3, a4, a5, a6, a7;
+              const int c0 = 2 * ks + (mi >> 1), c1 = c0 + 2;     // 16-byte chunks over d
+              ldsm_x4(a0, a1, a2, a3, rowk + (c0 >> 3) * (P * 128) + (((c0 & 7) ^ xt) << 4));
+              ldsm_x4(a4, a5, a6, a7, rowk + (c1 >> 3) * (P * 128) + (((c1 & 7) ^ xt) << 4));
+              mma_bf16(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              mma_bf16(sx, a4, a5, a6, a7, qb[ks + 1][0], qb[ks + 1][1]);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) x[j][i] = (s4[i] + sx[i]) * qscale_log2;
+          vsA[j] = vsB[j] = 0.0f;
+          if (FP8) {
+            const float kA = ksc[tkA[j]], kB = ksc[tkB[j]];
+            x[j][0] *= kA; x[j][1] *= kA; x[j][2] *= kB; x[j][3] *= kB;
+            vsA[j] = vsc[tkA[j]];
+            vsB[j] = vsc[tkB[j]];
+          }
+          if (nvalid < tb + 16) {          // the tail of a request's last page
+            if (tkA[j] >= nvalid) { x[j][0] = x[j][1] = -INFINITY; vsA[j] = 0.0f; }
+            if (tkB[j] >= nvalid) { x[j][2] = x[j][3] = -INFINITY; vsB[j] = 0.0f; }
+          }
+        }
+        // per-head maxima over the step's tokens: the 8 lanes r4 = 0..7 of c
+        float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+        for (int j = 1; j < NB; ++j) {
+          mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][2]));
+          mx1 = fmaxf(mx1, fmaxf(x[j][1], x[j][3]));
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
+        const float corr0 = fast_exp2(m_run0 - mu0), corr1 = fast_exp2(m_run1 - mu1);
+        float oc0 = corr0, oc1 = corr1;
+        float vinv = 1.0f;
+        if (FP8) {
+          float vmax = fmaxf(vsA[0], vsB[0]);
+#pragma unroll
+          for (int j = 1; j < NB; ++j) vmax = fmaxf(vmax, fmaxf(vsA[j], vsB[j]));
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1)
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+          if (vmax >= vref) {
+            const float nref = __uint_as_float(((__float_as_uint(vmax) >> 23) + 1) << 23);
+            const float ratio = vref * pow2_rcp(nref);
+            oc0 *= ratio;
+            oc1 *= ratio;
+            vref = nref;
+          }
+          vinv = pow2_rcp(vref);
+        }
+        uint32_t b0[NB], b1[NB];
+        float ls0 = 0.0f, ls1 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          const float p0 = fast_exp2(x[j][0] - mu0), p1 = fast_exp2(x[j][1] - mu1);
+          const float p2 = fast_exp2(x[j][2] - mu0), p3 = fast_exp2(x[j][3] - mu1);
+          uint32_t P0, P1;
+          if (FP8) {
+            ls0 += p0 + p2;
+            ls1 += p1 + p3;
+            const float wA = vsA[j] * vinv, wB = vsB[j] * vinv;
+            P0 = pack_f16(p0 * wA, p1 * wA);
+            P1 = pack_f16(p2 * wB, p3 * wB);
+          } else {
+            const float q0 = bf16_round(p0), q1 = bf16_round(p1);
+            const float q2 = bf16_round(p2), q3 = bf16_round(p3);
+            ls0 += q0 + q2;
+            ls1 += q1 + q3;
+            P0 = pack_bf16(q0, q1);
+            P1 = pack_bf16(q2, q3);
+          }
+          // P^T as the B operand: each 8x8 half transposed across the warp
+          b0[j] = movmatrix_trans(P0);
+          b1[j] = movmatrix_trans(P1);
+        }
+        l_run0 = l_run0 * corr0 + ls0;
+        l_run1 = l_run1 * corr1 + ls1;
+        m_run0 = mn0;
+        m_run1 = mn1;
+        if (__any_sync(0xffffffffu, oc0 != 1.0f || oc1 != 1.0f)) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= oc0; o[mt][1] *= oc1; o[mt][2] *= oc0; o[mt][3] *= oc1;
+          }
+        }
+
+        // O^T += V^T P^T, 16 rows of d per MMA, the step's blocks in turn
+        if (FP8) {
+          // rows d = 16*mt + r4 and +8: the swizzle bits do not depend on mt
+          // (16*P*mt is a multiple of the swizzle period), so hoist them
+          uint32_t va0[NB], va1[NB];
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+            va0[j] = vb + swz(r4 * P + tb0 + 16 * j + 4 * c, C::kVSwz);
+            va1[j] = vb + swz((r4 + 8) * P + tb0 + 16 * j + 4 * c, C::kVSwz);
+          }
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              uint32_t w0 = lds32(va0[j] + mt * 16 * P);
+              uint32_t w1 = lds32(va1[j] + mt * 16 * P);
+              w0 = __funnelshift_l(w0, w0, rot);
+              w1 = __funnelshift_l(w1, w1, rot);
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x2x2(w0, a0, a2);
+              e4m3x4_to_f16x2x2(w1, a1, a3);
+              mma_f16(o[mt], a0, a1, a2, a3, b0[j], b1[j]);
+            }
+          }
+        } else {
+          const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              const int t = tb0 + 16 * j + (mi >> 1) * 8 + rr;
+              const int chunk = 2 * mt + (mi & 1);
+              const uint32_t addr =
+                  vb + (chunk >> 3) * (P * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_t(a0, a1, a2, a3, addr);
+              mma_bf16(o[mt], a0, a1, a2, a3, b0[j], b1[j]);
+            }
           }
         }
       }
-#pragma unroll
-      for (int jb = 0; jb < NB; ++jb) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          x[jb][i] = (FP8 ? s4[jb][i] : s4[jb][i] + sx[FP8 ? 0 : jb][i]) * qscale_log2;
-        const int tkA = 16 * jb + tauA, tkB = 16 * jb + tauB;
-        vsA[jb] = vsB[jb] = 0.0f;
-        if (FP8) {
-          const float kA = ksc[tkA], kB = ksc[tkB];
-          x[jb][0] *= kA; x[jb][1] *= kA; x[jb][2] *= kB; x[jb][3] *= kB;
-          vsA[jb] = vsc[tkA];
-          vsB[jb] = vsc[tkB];
-        }
-        if (nvalid < CT) {                // the tail of a request's last page
-          if (tkA >= nvalid) { x[jb][0] = x[jb][1] = -INFINITY; vsA[jb] = 0.0f; }
-          if (tkB >= nvalid) { x[jb][2] = x[jb][3] = -INFINITY; vsB[jb] = 0.0f; }
-        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[sb]);
+      ++pc;
+      if (dsc.x & kLast) {
+        fkind = (dsc.x & kFinal) ? 2 : 1;
+        funit = dsc.z;
       }
     }
-    // per-head maxima over the chunk's tokens: the 8 lanes r4 = 0..7 of c
-    float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
-#pragma unroll
-    for (int jb = 1; jb < NB; ++jb) {
-      mx0 = fmaxf(mx0, fmaxf(x[jb][0], x[jb][2]));
-      mx1 = fmaxf(mx1, fmaxf(x[jb][1], x[jb][3]));
-    }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
-    const float corr0 = fast_exp2(m_run0 - mu0), corr1 = fast_exp2(m_run1 - mu1);
-    float oc0 = corr0, oc1 = corr1;
-    float vinv = 1.0f;
-    if (FP8) {
-      float vmax = fmaxf(vsA[0], vsB[0]);
-#pragma unroll
-      for (int jb = 1; jb < NB; ++jb) vmax = fmaxf(vmax, fmaxf(vsA[jb], vsB[jb]));
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1)
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
-      if (vmax >= vref) {
-        const float nref = __uint_as_float(((__float_as_uint(vmax) >> 23) + 1) << 23);
-        const float ratio = vref * pow2_rcp(nref);
-        oc0 *= ratio;
-        oc1 *= ratio;
-        vref = nref;
-      }
-      vinv = pow2_rcp(vref);
-    }
-    uint32_t b0[NB], b1[NB];
-    float ls0 = 0.0f, ls1 = 0.0f;
-#pragma unroll
-    for (int jb = 0; jb < NB; ++jb) {
-      const float p0 = fast_exp2(x[jb][0] - mu0), p1 = fast_exp2(x[jb][1] - mu1);
-      const float p2 = fast_exp2(x[jb][2] - mu0), p3 = fast_exp2(x[jb][3] - mu1);
-      uint32_t P0, P1;
-      if (FP8) {
-        ls0 += p0 + p2;
-        ls1 += p1 + p3;
-        const float wA = vsA[jb] * vinv, wB = vsB[jb] * vinv;
-        P0 = pack_f16(p0 * wA, p1 * wA);
-        P1 = pack_f16(p2 * wB, p3 * wB);
-      } else {
-        const float q0 = bf16_round(p0), q1 = bf16_round(p1);
-        const float q2 = bf16_round(p2), q3 = bf16_round(p3);
-        ls0 += q0 + q2;
-        ls1 += q1 + q3;
-        P0 = pack_bf16(q0, q1);
-        P1 = pack_bf16(q2, q3);
-      }
-      // P^T as the B operand: each 8x8 half transposed across the warp
-      b0[jb] = movmatrix_trans(P0);
-      b1[jb] = movmatrix_trans(P1);
-    }
-    l_run0 = l_run0 * corr0 + ls0;
-    l_run1 = l_run1 * corr1 + ls1;
-    m_run0 = mn0;
-    m_run1 = mn1;
-    if (__any_sync(0xffffffffu, oc0 != 1.0f || oc1 != 1.0f)) {
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= oc0; o[mt][1] *= oc1; o[mt][2] *= oc0; o[mt][3] *= oc1;
-      }
-    }
-
-    // O^T += V^T P^T, 16 rows of d per MMA; per row tile the chunk's blocks
-    if (FP8) {
-      // rows d = 16*mt + r4 and +8: the swizzle bits do not depend on mt
-      // (16*CT*mt is a multiple of the swizzle period), so hoist them
-      uint32_t va0[NB], va1[NB];
-#pragma unroll
-      for (int jb = 0; jb < NB; ++jb) {
-        va0[jb] = vb + swz(r4 * CT + 16 * jb + 4 * c, C::kVSwz);
-        va1[jb] = vb + swz((r4 + 8) * CT + 16 * jb + 4 * c, C::kVSwz);
-      }
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-#pragma unroll
-        for (int jb = 0; jb < NB; ++jb) {
-          uint32_t w0 = lds32(va0[jb] + mt * 16 * CT);
-          uint32_t w1 = lds32(va1[jb] + mt * 16 * CT);
-          w0 = __funnelshift_l(w0, w0, rot);
-          w1 = __funnelshift_l(w1, w1, rot);
-          uint32_t a0, a1, a2, a3;
-          e4m3x4_to_f16x2x2(w0, a0, a2);
-          e4m3x4_to_f16x2x2(w1, a1, a3);
-          mma_f16(o[mt], a0, a1, a2, a3, b0[jb], b1[jb]);
-        }
-      }
-    } else {
-      const int mi = lane >> 3, rr = lane & 7;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-#pragma unroll
-        for (int jb = 0; jb < NB; ++jb) {
-          const int t = 16 * jb + (mi >> 1) * 8 + rr;
-          const int chunk = 2 * mt + (mi & 1);
-          const uint32_t addr =
-              vb + (chunk >> 3) * (CT * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(a0, a1, a2, a3, addr);
-          mma_bf16(o[mt], a0, a1, a2, a3, b0[jb], b1[jb]);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[sb]);
+  flushes:
+    if (fkind == 1 && !flush()) break;
+    if (fkind == 2 && !final_flush(funit)) break;
   }
-  if (done) final_flush(u_last);
 }
 
 // ---------------------------------------------------------------------------
@@ -1139,7 +1120,7 @@ size_t decode_smem() {
 // CTAs of one wave: resident CTAs per SM (the configuration's target, or
 // what the occupancy calculator grants, whichever is lower) x SMs, cut so
 // that every CTA gets at least two tiles and no unit more than 130 pieces.
-template <bool FP8, int P>
+template <bool FP8, int P, bool HT>
 int decode_grid(const Dims& d, int n_layers, int num_sms) {
   // per device: the occupancy calculator's answer depends on the GPU
   static std::atomic<int> occ_of[kMaxDevices];
@@ -1147,7 +1128,8 @@ int decode_grid(const Dims& d, int n_layers, int num_sms) {
   int occ = slot.load(std::memory_order_relaxed);
   if (occ < 1) {
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<FP8, P>, kDecodeThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<FP8, P, HT>,
+                                                      kDecodeThreads,
                                                       decode_smem<FP8, P>()) != cudaSuccess)
       o = 1;
     occ = o < 1 ? 1 : (o > Cfg<FP8, P>::kCtasPerSm ? Cfg<FP8, P>::kCtasPerSm : o);
@@ -1161,37 +1143,34 @@ int decode_grid(const Dims& d, int n_layers, int num_sms) {
   return n < 1 ? 1 : (int)n;
 }
 
-template <bool FP8, int P>
+template <bool FP8, int P, bool HT>
 cudaError_t launch_decode_t(const DecodeArgs& a, DecodeParams& p, cudaStream_t s) {
   const Dims& d = *a.d;
   const ssa_cache& c = *a.c;
   CUtensorMap tmK, tmV;
   const uint64_t rows_tok = (uint64_t)d.Lyr * d.S * d.Hkv * P;
   bool ok;
-  constexpr int CT = Cfg<FP8, P>::kCT;     // tokens per chunk (one TMA box)
   if (FP8) {
-    ok = make_tmap(&tmK, c.k_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kD, rows_tok, kD, CT,
+    ok = make_tmap(&tmK, c.k_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kD, rows_tok, kD, P,
                    CU_TENSOR_MAP_SWIZZLE_128B);
-    // V pages are d-major: rows of P token bytes; a chunk is a CT-byte column
-    // band of the page's 128 rows
-    const CUtensorMapSwizzle vsw = CT >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                 : CT == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
-                                 : CT == 32  ? CU_TENSOR_MAP_SWIZZLE_32B
-                                             : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUtensorMapSwizzle vsw = P >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : P == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : P == 32  ? CU_TENSOR_MAP_SWIZZLE_32B
+                                            : CU_TENSOR_MAP_SWIZZLE_NONE;
     ok = ok && make_tmap(&tmV, c.v_pool, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, P,
-                         (uint64_t)d.Lyr * d.S * d.Hkv * kD, CT, kD, vsw);
+                         (uint64_t)d.Lyr * d.S * d.Hkv * kD, P, kD, vsw);
   } else {
-    ok = make_tmap(&tmK, c.k_pool, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, rows_tok, 64, CT,
+    ok = make_tmap(&tmK, c.k_pool, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, rows_tok, 64, P,
                    CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && make_tmap(&tmV, c.v_pool, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, rows_tok, 64, CT,
+    ok = ok && make_tmap(&tmV, c.v_pool, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, rows_tok, 64, P,
                          CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return cudaErrorInvalidValue;
   const size_t smem = decode_smem<FP8, P>();
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP8, P>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP8, P, HT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int n = decode_grid<FP8, P>(d, a.n_layers, a.num_sms);
+  const int n = decode_grid<FP8, P, HT>(d, a.n_layers, a.num_sms);
   if (n > decode_max_ctas(d, a.num_sms)) return cudaErrorInvalidValue;   // workspace bound
   p.w = d.max_selected();
   const long long T = (long long)a.n_layers * d.B * d.Hkv * p.w;
@@ -1199,7 +1178,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, DecodeParams& p, cudaStream_t s
   p.T = (int)T;
   p.tq = p.T / n;
   p.tr = p.T % n;
-  e = launch_pdl(decode_kernel<FP8, P>, dim3(n), dim3(kDecodeThreads), smem, s, p, tmK, tmV);
+  e = launch_pdl(decode_kernel<FP8, P, HT>, dim3(n), dim3(kDecodeThreads), smem, s, p, tmK, tmV);
   count_launch();
   return e;
 }
@@ -1248,15 +1227,23 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   p.v_mir = static_cast<const uint8_t*>(c.v_mirror);
   p.ks_mir = c.k_scale_mirror;
   p.vs_mir = c.v_scale_mirror;
-  switch (d.P * 2 + d.fp8) {
-    case 32: return launch_decode_t<false, 16>(a, p, s);
-    case 33: return launch_decode_t<true, 16>(a, p, s);
-    case 64: return launch_decode_t<false, 32>(a, p, s);
-    case 65: return launch_decode_t<true, 32>(a, p, s);
-    case 128: return launch_decode_t<false, 64>(a, p, s);
-    case 129: return launch_decode_t<true, 64>(a, p, s);
-    case 256: return launch_decode_t<false, 128>(a, p, s);
-    case 257: return launch_decode_t<true, 128>(a, p, s);
+  switch ((d.P * 2 + d.fp8) * 2 + (a.host_tail ? 1 : 0)) {
+    case 64: return launch_decode_t<false, 16, false>(a, p, s);
+    case 65: return launch_decode_t<false, 16, true>(a, p, s);
+    case 66: return launch_decode_t<true, 16, false>(a, p, s);
+    case 67: return launch_decode_t<true, 16, true>(a, p, s);
+    case 128: return launch_decode_t<false, 32, false>(a, p, s);
+    case 129: return launch_decode_t<false, 32, true>(a, p, s);
+    case 130: return launch_decode_t<true, 32, false>(a, p, s);
+    case 131: return launch_decode_t<true, 32, true>(a, p, s);
+    case 256: return launch_decode_t<false, 64, false>(a, p, s);
+    case 257: return launch_decode_t<false, 64, true>(a, p, s);
+    case 258: return launch_decode_t<true, 64, false>(a, p, s);
+    case 259: return launch_decode_t<true, 64, true>(a, p, s);
+    case 512: return launch_decode_t<false, 128, false>(a, p, s);
+    case 513: return launch_decode_t<false, 128, true>(a, p, s);
+    case 514: return launch_decode_t<true, 128, false>(a, p, s);
+    case 515: return launch_decode_t<true, 128, true>(a, p, s);
     default: return cudaErrorInvalidValue;
   }
 }

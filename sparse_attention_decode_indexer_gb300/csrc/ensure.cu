@@ -58,6 +58,9 @@ struct EnsureParams {
   int32_t* phys;         // [n_layers][B][W] or null: the remapped table (a5 fused)
   int32_t* status;
   int layer0, Lp, S, B, W, nmax, N2, mstride;
+  // layers whose selections one state serves: 1 (one CTA per layer), or the
+  // call's layer count (one CTA; the first layer's state, shared residency)
+  int nsel;
   int has_mirror;
   // 0: the step's ensure (epoch = clock; hits touched; every miss bound; clock
   // advances).  1: a preload after the step's ensure (epoch = clock - 1;
@@ -102,7 +105,7 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
 
   const int li = blockIdx.x, layer = p.layer0 + li;
   const int tid = threadIdx.x, nt = blockDim.x;
-  const int BW = p.B * p.W;
+  const int BW = p.B * p.W * p.nsel;        // selection entries this state serves
   int32_t* slot_of = p.slot_of + (size_t)layer * p.Lp;
   int32_t* page_of = p.page_of + (size_t)layer * p.S;
   int32_t* last_use = p.last_use + (size_t)layer * p.S;
@@ -115,8 +118,8 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
   // 1. the distinct selected logical ids, ascending, in ids[] (0xFFFFFFFF
   //    after them)
   auto selected_id = [&](int i) -> uint32_t {        // entry i of the batch's selection
-    const int b = i / p.W;
-    const int pg = p.sel[((size_t)li * p.B + b) * p.W + (i - b * p.W)];
+    const int b = (i / p.W) % p.B;             // layer li + i / (B*W) in shared residency
+    const int pg = p.sel[(size_t)li * p.B * p.W + i];
     if (pg < 0) return 0xFFFFFFFFu;
     const int id = pg < p.nmax ? p.bt[(size_t)b * p.nmax + pg] : -1;
     if (id >= 0 && id < p.Lp) return (uint32_t)id;
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
     int32_t* phys = p.phys + (size_t)li * BW;
     const int32_t* sel = p.sel + (size_t)li * BW;
     for (int i = tid; i < BW; i += nt) {
-      const int b = i / p.W;
+      const int b = (i / p.W) % p.B;
       const int pg = sel[i];
       int out = -1;
       if (pg >= 0) {
@@ -364,6 +367,7 @@ struct CopyParams {
   float *k_scale, *v_scale;
   const int32_t *miss_page, *miss_slot, *n_miss;
   int layer0, Lp, S, BW, P, fp8;
+  int shared;             // one miss list (the first layer's) for every layer
   long long page_bytes;   // one page, all KV heads
 };
 
@@ -371,9 +375,10 @@ __global__ void __launch_bounds__(kCopyThreads) miss_copy_kernel(CopyParams p) {
   pdl_trigger();
   pdl_wait();
   const int entry = blockIdx.y, li = blockIdx.z, layer = p.layer0 + li;
-  if (entry >= p.n_miss[li] || p.k_mir == nullptr) return;
-  const int pg = p.miss_page[(size_t)li * p.BW + entry];
-  const int slot = p.miss_slot[(size_t)li * p.BW + entry];
+  const int lst = p.shared ? 0 : li;          // the miss list this layer copies
+  if (entry >= p.n_miss[lst] || p.k_mir == nullptr) return;
+  const int pg = p.miss_page[(size_t)lst * p.BW + entry];
+  const int slot = p.miss_slot[(size_t)lst * p.BW + entry];
   if (pg < 0 || pg >= p.Lp || slot < 0 || slot >= p.S) return;
   const long long pb16 = p.page_bytes / 16;
   const long long sc16 = p.fp8 ? (long long)p.P * 4 / 16 : 0;
@@ -442,9 +447,9 @@ __global__ void remap_kernel(const int32_t* slot_of, const int32_t* sel, const i
 
 }  // namespace
 
-int ensure_sort_width(const Dims& d) {
+int ensure_sort_width(const Dims& d, int nsel) {
   int n = 2;
-  while (n < d.B * d.W) n <<= 1;
+  while (n < d.B * d.W * nsel) n <<= 1;
   return n;
 }
 
@@ -453,15 +458,16 @@ namespace {
 cudaError_t launch_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
                          const int32_t* sel, int width, int preload, const int32_t* bt,
                          int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
-                         int32_t* phys, int32_t* status, cudaStream_t s) {
+                         int32_t* phys, int32_t* status, cudaStream_t s, bool shared = false) {
   EnsureParams p{};
   p.phys = phys;
+  p.nsel = shared ? n_layers : 1;
   p.slot_of = c.slot_of; p.page_of = c.page_of; p.last_use = c.last_use; p.clock = c.clock;
   p.sel = sel; p.bt = bt; p.miss_page = miss_page; p.miss_slot = miss_slot; p.n_miss = n_miss;
   p.status = status;
   p.layer0 = layer0; p.Lp = d.Lp; p.S = d.S; p.B = d.B; p.W = width; p.nmax = d.nmax;
-  p.N2 = ensure_sort_width(d);
-  p.mstride = d.B * d.W;
+  p.N2 = ensure_sort_width(d, p.nsel);
+  p.mstride = d.B * d.W * p.nsel;
   p.preload = preload;
   p.has_mirror = c.k_mirror != nullptr;
   // small batches and pools: 256 threads (cheaper barriers); else 1024
@@ -480,7 +486,7 @@ cudaError_t launch_state(const Dims& d, const ssa_cache& c, int layer0, int n_la
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = launch_pdl(k, dim3(n_layers), dim3(threads), smem, s, p);
+  cudaError_t e = launch_pdl(k, dim3(shared ? 1 : n_layers), dim3(threads), smem, s, p);
   count_launch();
   return e;
 }
@@ -495,6 +501,14 @@ cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, i
                       phys, status, s);
 }
 
+cudaError_t launch_ensure_state_shared(const Dims& d, const ssa_cache& c, int layer0,
+                                       int n_layers, const int32_t* sel, const int32_t* bt,
+                                       int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
+                                       int32_t* phys, int32_t* status, cudaStream_t s) {
+  return launch_state(d, c, layer0, n_layers, sel, d.W, 0, bt, miss_page, miss_slot, n_miss,
+                      phys, status, s, true);
+}
+
 cudaError_t launch_preload_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
                                  const int32_t* cand, int width, const int32_t* bt,
                                  int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
@@ -505,7 +519,8 @@ cudaError_t launch_preload_state(const Dims& d, const ssa_cache& c, int layer0, 
 
 cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
                              const int32_t* miss_page, const int32_t* miss_slot,
-                             const int32_t* n_miss, int32_t* status, cudaStream_t s) {
+                             const int32_t* n_miss, int32_t* status, cudaStream_t s,
+                             bool shared) {
   (void)status;
   if (c.k_mirror == nullptr) return cudaSuccess;   // nothing to fetch from (flagged by ensure)
   CopyParams p{};
@@ -515,7 +530,9 @@ cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int 
   p.k_pool = static_cast<uint8_t*>(c.k_pool); p.v_pool = static_cast<uint8_t*>(c.v_pool);
   p.k_scale = c.k_scale; p.v_scale = c.v_scale;
   p.miss_page = miss_page; p.miss_slot = miss_slot; p.n_miss = n_miss;
-  p.layer0 = layer0; p.Lp = d.Lp; p.S = d.S; p.BW = d.B * d.W; p.P = d.P; p.fp8 = d.fp8;
+  p.layer0 = layer0; p.Lp = d.Lp; p.S = d.S; p.P = d.P; p.fp8 = d.fp8;
+  p.shared = shared ? 1 : 0;
+  p.BW = d.B * d.W * (shared ? n_layers : 1);   // list stride and entries per list
   p.page_bytes = (long long)d.page_bytes();
   const long long total16 = 2 * p.page_bytes / 16 + (d.fp8 ? 2LL * d.P * 4 / 16 : 0);
   dim3 grid((unsigned)((total16 + kCopyChunk - 1) / kCopyChunk), p.BW, n_layers);

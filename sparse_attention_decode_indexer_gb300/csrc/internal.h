@@ -55,9 +55,19 @@ cudaError_t launch_preload_state(const Dims& d, const ssa_cache& c, int layer0, 
                                  const int32_t* cand, int width, const int32_t* bt,
                                  int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
                                  int32_t* status, cudaStream_t s);
+// shared: one miss list (residency shared by the call's layers) copied into
+// every layer's pool
 cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
                              const int32_t* miss_page, const int32_t* miss_slot,
-                             const int32_t* n_miss, int32_t* status, cudaStream_t s);
+                             const int32_t* n_miss, int32_t* status, cudaStream_t s,
+                             bool shared = false);
+// Residency shared by the layers of a call: one CTA ensures the union of the
+// layers' selections sel [n_layers][B][W] on layer0's state; phys for every
+// layer; the miss list [n_layers * B * W], its count n_miss[0].
+cudaError_t launch_ensure_state_shared(const Dims& d, const ssa_cache& c, int layer0,
+                                       int n_layers, const int32_t* sel, const int32_t* bt,
+                                       int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
+                                       int32_t* phys, int32_t* status, cudaStream_t s);
 cudaError_t launch_remap(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
                          const int32_t* sel, const int32_t* bt, int32_t* phys,
                          int32_t* status, cudaStream_t s);

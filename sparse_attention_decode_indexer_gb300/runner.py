@@ -22,14 +22,14 @@ import math
 
 import torch
 
-from . import (KVCache, Layout, ssa_ensure_remap, ssa_ensure_resident, ssa_index_topk,
-               ssa_lru_init, ssa_prefetch_pages, ssa_remap_block_table, ssa_sparse_paged_decode,
-               ssa_store_kv_mirror, ssa_workspace_size)
+from . import (KVCache, Layout, ssa_ensure_remap, ssa_ensure_remap_shared, ssa_ensure_resident,
+               ssa_index_topk, ssa_lru_init, ssa_prefetch_pages, ssa_remap_block_table,
+               ssa_sparse_paged_decode, ssa_store_kv_mirror, ssa_workspace_size)
 
 
 class DecodeRunner:
     def __init__(self, layout: Layout, host_tier: bool, identity: bool, block_table, seq_lens,
-                 device="cuda", preload_width: int = 0):
+                 device="cuda", preload_width: int = 0, shared_residency: bool = False):
         self.layout = layout
         self.cache = KVCache(layout, host_tier, device)
         L, B, W = layout.n_layers, layout.batch, layout.max_sel
@@ -51,6 +51,9 @@ class DecodeRunner:
                               device=device)
         self.sm_scale = 1.0 / math.sqrt(layout.head_dim)
         ssa_lru_init(self.cache, identity)
+        # one LRU state for all layers (the first layer's), each miss copied
+        # for every layer; layer-batched steps only
+        self.shared_residency = bool(shared_residency)
         self.preload_width = 0
         if preload_width:
             self.enable_preload(preload_width)
@@ -84,7 +87,11 @@ class DecodeRunner:
         ssa_index_topk(c, layer0, n_layers, q, self.block_table, self.seq_lens, self.sel[sl],
                        self.n_sel[sl], self.scores[sl] if keep_scores else None, self.status,
                        self.ws)
-        if fused:
+        if fused and self.shared_residency:
+            ssa_ensure_remap_shared(c, layer0, n_layers, self.sel[sl], self.block_table,
+                                    self.phys[sl], self.miss_page[sl], self.miss_slot[sl],
+                                    self.n_miss[sl], self.status, self.ws)
+        elif fused:
             ssa_ensure_remap(c, layer0, n_layers, self.sel[sl], self.block_table, self.phys[sl],
                              self.miss_page[sl], self.miss_slot[sl], self.n_miss[sl],
                              self.status, self.ws)

@@ -116,3 +116,29 @@ def test_lost_arrival_ends_in_timeout_status_not_a_hang():
     # the context is still usable
     x = torch.arange(10, device="cuda").sum()
     assert int(x.item()) == 45
+
+
+def test_attention_is_bitwise_deterministic_across_calls():
+    # units split across CTAs are merged by whichever piece finishes last;
+    # both merge paths do the same arithmetic, so repeated calls agree bit
+    # for bit (many units of a few pages, ragged lengths: many merges)
+    import sparse_attention_decode_indexer_gb300 as ssa
+    w = wl.Workload("det", batch=24, n_layers=2, ctx=64 * 30,
+                    seq_lens=tuple(64 * 30 if i % 3 == 0 else (i * 211) % (64 * 30) + 1
+                                   for i in range(24)),
+                    page_size=64, n_q_heads=16, n_kv_heads=2, head_dim=128, fp8=True,
+                    block_topk=8, pool_slots=None, seed=311)
+    run = gpu_runner(w)
+    prefill(w, run, None, [])
+    q = torch.from_numpy(np.stack([wl.queries(w, l)[0] for l in range(2)]).view(np.int16)).view(
+        torch.bfloat16).cuda()
+    run.step(q)
+    torch.cuda.synchronize()
+    ref = run.out.clone()
+    for _ in range(6):
+        out = torch.empty_like(run.out)
+        ssa.ssa_sparse_paged_decode(run.cache, 0, 2, q, run.sel, run.phys, run.seq_lens,
+                                    run.sm_scale, out, run.status, run.ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    assert int(run.status.item()) == 0

@@ -420,7 +420,7 @@ def run_ours(args, rank: int, world: int, dist):
     W, K = args.warmup, args.steps
     H_max = args.host_warmup if args.host_warmup >= 0 else (300 if w.host_tier else 0)
     run = build_runner(w, rank, prefill_now=False)   # graphs first, then one prefill
-    n_total = H_max + W + 4 * K + (8 * K + 100 if w.host_tier else 0)
+    n_total = H_max + W + 4 * K + (10 * K + 140 if w.host_tier else 0)
     q_all = queries_all(w, n_total)
     q_cur = q_all[0].clone()
     flush_w = torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB > L2
@@ -628,7 +628,9 @@ def run_ours(args, rank: int, world: int, dist):
                "ms_per_step": 1e3 * tot / K,
                "path": "DecodeRunner.step (4 C-ABI calls, direct launches) + pinned H2D q / D2H out"}
 
-    preload = host_tail = None
+    preload = host_tail = fetch = None
+    if w.host_tier:
+        fetch = time_fetch_in_attention(w, run, q_all, q_cur, H + W + 12 * K + 100, K, flush_l2)
     if w.host_tier and not args.no_legs:
         preload = time_preload(w, run, q_all, H + W + 4 * K, K, flush_l2)
         host_tail = time_host_tail(w, run, q_all, H + W + 8 * K + 8, K, flush_l2)
@@ -703,6 +705,8 @@ def run_ours(args, rank: int, world: int, dist):
         line["e2e"] = e2e
     if store is not None:
         line["store"] = store
+    if fetch is not None:
+        line["fetch_in_attention"] = fetch
     if preload is not None:
         line["preload"] = preload
     if host_tail is not None:
@@ -767,6 +771,86 @@ def time_preload(w: wl.Workload, run, q_all, t0: int, K: int, flush_l2):
                    "stream; (a) per-step regions after an L2 flush, closed after the preload; "
                    "(b) K steps back to back")
     return out
+
+
+def time_fetch_in_attention(w: wl.Workload, run, q_all, q_cur, t0: int, K: int, flush_l2):
+    """The miss fetch folded into the attention (ssa_ensure_remap_deferred +
+    ssa_sparse_paged_decode_fetch) against the headline step's copy-then-
+    attend, timed the same way: one CUDA graph per step with events at its
+    ends, L2 flushed before each replay; stage times from a second graph
+    with events between the stages."""
+    import torch
+    import sparse_attention_decode_indexer_gb300 as ssa
+    L, c = w.n_layers, run.cache
+
+    def st_index():
+        ssa.ssa_index_topk(c, 0, L, q_cur, run.block_table, run.seq_lens, run.sel, run.n_sel,
+                           None, run.status, run.ws)
+
+    def st_state():
+        ssa.ssa_ensure_remap_deferred(c, 0, L, run.sel, run.block_table, run.phys,
+                                      run.miss_page, run.miss_slot, run.n_miss, run.status,
+                                      run.ws)
+
+    def st_attend():
+        ssa.ssa_sparse_paged_decode_fetch(c, 0, L, q_cur, run.sel, run.phys, run.block_table,
+                                          run.seq_lens, run.sm_scale, run.out, run.status,
+                                          run.ws)
+
+    stages = [("index_topk", st_index), ("ensure_state", st_state), ("decode_fetch", st_attend)]
+    for _, f in stages:
+        f()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+    g_plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plain, stream=s):
+        pev[0].record()
+        for _, f in stages:
+            f()
+        pev[1].record()
+    sev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(stages) + 1)]
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=s):
+        sev[0].record()
+        for i, (_, f) in enumerate(stages):
+            f()
+            sev[i + 1].record()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    t = t0
+    for _ in range(20):                        # the host link settles as for the headline
+        flush_l2()
+        q_cur.copy_(q_all[t]); t += 1
+        g_plain.replay()
+    torch.cuda.synchronize()
+    ms, miss = [], 0
+    for _ in range(K):
+        flush_l2()
+        q_cur.copy_(q_all[t]); t += 1
+        g_plain.replay()
+        pev[1].synchronize()
+        ms.append(pev[0].elapsed_time(pev[1]))
+        miss += int(run.n_miss.sum().item())
+    rows = []
+    for _ in range(K):
+        flush_l2()
+        q_cur.copy_(q_all[t]); t += 1
+        g_step.replay()
+        sev[-1].synchronize()
+        rows.append([sev[i].elapsed_time(sev[i + 1]) for i in range(len(stages))])
+    st = int(run.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the fetch-in-attention leg")
+    step_ms = statistics.mean(ms)
+    return {"ms_per_step": step_ms, "value": L * w.batch / (step_ms * 1e-3),
+            "stages_us": {name: 1e3 * statistics.mean(r[i] for r in rows)
+                          for i, (name, _) in enumerate(stages)},
+            "misses_per_step": miss / K,
+            "note": "index -> ensure state + remap (misses marked) -> attention that reads the "
+                    "marked pages from the host mirror and writes them into their slots; "
+                    "graph per step, L2 flushed before each"}
 
 
 def time_host_tail(w: wl.Workload, run, q_all, t0: int, K: int, flush_l2):

@@ -254,6 +254,35 @@ int ssa_ensure_remap(const ssa_layout *lay, const ssa_cache *c, int layer0, int 
                      int32_t *status, void *ws, ssa_stream_t stream);
 
 /*
+ * The miss fetch folded into the attention: ssa_ensure_remap_deferred runs
+ * the ensure's state update and remap (a3, a5) but copies nothing; its phys
+ * marks each page this call bound (a miss) as -2 - slot.  Then
+ * ssa_sparse_paged_decode_fetch runs the attention on that phys: a marked
+ * page is read from the pinned host mirror inside the attention kernel (the
+ * host-tail path), used, and written into its slot as it streams past, so
+ * the host-link reads overlap the attention over the resident pages instead
+ * of preceding it (FreeToken PR #499, "Design": ensure, then copy, then
+ * attend; vLLM RFC #33980, "Motivation": the load time is what has to be
+ * hidden).  The residency state, the miss lists, the pool bytes afterwards
+ * and the outputs are those of ssa_ensure_remap + ssa_sparse_paged_decode.
+ * Between the two calls the marked slots hold stale bytes: nothing else may
+ * read them, and the pair must not be split across other calls on the
+ * cache.  Both require the host mirror (SSA_ERR_NO_MIRROR).
+ *   phys [n_layers][B][W] int32 out / in: slot, -2 - slot (marked), or -1
+ *   block_table (fetch): as for ssa_index_topk, for the marked pages' ids
+ */
+int ssa_ensure_remap_deferred(const ssa_layout *lay, const ssa_cache *c, int layer0,
+                              int n_layers, const int32_t *sel, const int32_t *block_table,
+                              int32_t *phys, int32_t *miss_page_opt, int32_t *miss_slot_opt,
+                              int32_t *n_miss_opt, int32_t *status, void *ws,
+                              ssa_stream_t stream);
+int ssa_sparse_paged_decode_fetch(const ssa_layout *lay, const ssa_cache *c, int layer0,
+                                  int n_layers, const void *q, const int32_t *sel,
+                                  const int32_t *phys, const int32_t *block_table,
+                                  const int32_t *seq_lens, float sm_scale, void *out,
+                                  int32_t *status, void *ws, ssa_stream_t stream);
+
+/*
  * Residency shared by the layers of a call (FreeToken PR #499, "Design": one
  * launch copies a page's K and V for all the sparse-attention layers).  The
  * layers [layer0, layer0 + n_layers) share ONE LRU state, layer0's slot_of /

@@ -36,7 +36,8 @@ EXPORTS = ("ssa_workspace_size", "ssa_lru_init", "ssa_store_kv_mirror", "ssa_ind
            "ssa_status_str", "ssa_last_cuda_error", "ssa_launch_count",
            "ssa_index_topk_static_scratch", "ssa_selftest_bounded_wait", "ssa_host_read_probe",
            "ssa_prefetch_pages", "ssa_ensure_remap", "ssa_sparse_paged_decode_host_tail",
-           "ssa_ensure_remap_shared")
+           "ssa_ensure_remap_shared", "ssa_ensure_remap_deferred",
+           "ssa_sparse_paged_decode_fetch")
 
 
 class SsaError(RuntimeError):
@@ -97,6 +98,11 @@ def lib():
         L.ssa_sparse_paged_decode_host_tail.argtypes = ([P(SsaLayout), P(SsaCache), i32, i32, vp,
                                                          vp, vp, vp, ctypes.c_float, vp, vp, vp,
                                                          vp])
+        L.ssa_ensure_remap_deferred.restype = i32
+        L.ssa_ensure_remap_deferred.argtypes = [P(SsaLayout), P(SsaCache), i32, i32] + [vp] * 9
+        L.ssa_sparse_paged_decode_fetch.restype = i32
+        L.ssa_sparse_paged_decode_fetch.argtypes = ([P(SsaLayout), P(SsaCache), i32, i32, vp, vp,
+                                                     vp, vp, vp, ctypes.c_float, vp, vp, vp, vp])
         L.ssa_ensure_remap_shared.restype = i32
         L.ssa_ensure_remap_shared.argtypes = [P(SsaLayout), P(SsaCache), i32, i32] + [vp] * 9
         L.ssa_ensure_remap.restype = i32
@@ -260,6 +266,27 @@ def ssa_ensure_remap(cache: KVCache, layer0: int, n_layers: int, sel, block_tabl
                                   n_layers, _ptr(sel), _ptr(block_table), _ptr(phys),
                                   _ptr(miss_page), _ptr(miss_slot), _ptr(n_miss), _ptr(status),
                                   _ptr(ws), _stream(stream)))
+
+
+def ssa_ensure_remap_deferred(cache: KVCache, layer0: int, n_layers: int, sel, block_table, phys,
+                              miss_page, miss_slot, n_miss, status, ws, stream=None):
+    """The ensure's state update and remap without the copy: misses marked
+    -2 - slot in phys, for ssa_sparse_paged_decode_fetch to fetch."""
+    _check(lib().ssa_ensure_remap_deferred(ctypes.byref(cache._lay), ctypes.byref(cache.c),
+                                           layer0, n_layers, _ptr(sel), _ptr(block_table),
+                                           _ptr(phys), _ptr(miss_page), _ptr(miss_slot),
+                                           _ptr(n_miss), _ptr(status), _ptr(ws), _stream(stream)))
+
+
+def ssa_sparse_paged_decode_fetch(cache: KVCache, layer0: int, n_layers: int, q, sel, phys,
+                                  block_table, seq_lens, sm_scale: float, out, status, ws,
+                                  stream=None):
+    """Attention that fetches the pages ssa_ensure_remap_deferred marked from
+    the host mirror and writes them into their slots as it goes."""
+    _check(lib().ssa_sparse_paged_decode_fetch(
+        ctypes.byref(cache._lay), ctypes.byref(cache.c), layer0, n_layers, _ptr(q), _ptr(sel),
+        _ptr(phys), _ptr(block_table), _ptr(seq_lens), float(sm_scale), _ptr(out), _ptr(status),
+        _ptr(ws), _stream(stream)))
 
 
 def ssa_ensure_remap_shared(cache: KVCache, layer0: int, n_layers: int, sel, block_table, phys,

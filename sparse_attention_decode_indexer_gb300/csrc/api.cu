@@ -256,6 +256,30 @@ int ssa_ensure_remap(const ssa_layout* lay, const ssa_cache* c, int layer0, int 
                      n_miss_opt, phys, status, ws, stream);
 }
 
+int ssa_ensure_remap_deferred(const ssa_layout* lay, const ssa_cache* c, int layer0,
+                              int n_layers, const int32_t* sel, const int32_t* block_table,
+                              int32_t* phys, int32_t* miss_page_opt, int32_t* miss_slot_opt,
+                              int32_t* n_miss_opt, int32_t* status, void* ws,
+                              ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if ((r = check_cache(d, c))) return r;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (!sel || !block_table || !phys) return SSA_ERR_INVALID_ARG;
+  if (!has_mirror(d, c)) return SSA_ERR_NO_MIRROR;        // the attention fetches from it
+  const long long need = (long long)d.B * d.W < d.Lp ? (long long)d.B * d.W : d.Lp;
+  if (d.S < need) return SSA_ERR_POOL_TOO_SMALL;
+  if (!ws && (!miss_page_opt || !miss_slot_opt || !n_miss_opt)) return SSA_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(d);
+  int32_t* mp = miss_page_opt ? miss_page_opt : at<int32_t>(ws, w.miss_page);
+  int32_t* ms = miss_slot_opt ? miss_slot_opt : at<int32_t>(ws, w.miss_slot);
+  int32_t* nm = n_miss_opt ? n_miss_opt : at<int32_t>(ws, w.n_miss);
+  cudaError_t e = launch_ensure_state_deferred(d, *c, layer0, n_layers, sel, block_table, mp, ms,
+                                               nm, phys, status, (cudaStream_t)stream);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
 int ssa_ensure_remap_shared(const ssa_layout* lay, const ssa_cache* c, int layer0,
                             int n_layers, const int32_t* sel, const int32_t* block_table,
                             int32_t* phys, int32_t* miss_page_opt, int32_t* miss_slot_opt,
@@ -331,21 +355,24 @@ int ssa_remap_block_table(const ssa_layout* lay, const ssa_cache* c, int layer0,
   return e == cudaSuccess ? SSA_OK : fail_cuda(e);
 }
 
+// mode: 0 resident (phys), 1 host tail (block_table, slot_of), 2 fetch (phys
+// with deferred misses marked, block_table)
 static int decode_impl(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
                        const void* q, const int32_t* sel, const int32_t* phys,
                        const int32_t* block_table, const int32_t* seq_lens, float sm_scale,
-                       void* out, int32_t* status, void* ws, ssa_stream_t stream) {
+                       void* out, int32_t* status, void* ws, ssa_stream_t stream, int mode) {
   Dims d;
   int r = check_layout(lay, d);
   if (r) return r;
   if (!c || !c->k_pool || !c->v_pool || (d.fp8 && (!c->k_scale || !c->v_scale)))
     return SSA_ERR_INVALID_ARG;
   if ((r = check_range(d, layer0, n_layers))) return r;
-  const bool host_tail = block_table != nullptr;
+  const bool host_tail = mode == 1, fetch = mode == 2;
   if (!q || !sel || (!phys && !host_tail) || !seq_lens || !out) return SSA_ERR_INVALID_ARG;
+  if ((host_tail || fetch) && !block_table) return SSA_ERR_INVALID_ARG;
   if (!ws) return SSA_ERR_INVALID_ARG;
-  if (host_tail) {
-    if (!c->slot_of) return SSA_ERR_INVALID_ARG;
+  if (host_tail || fetch) {
+    if (host_tail && !c->slot_of) return SSA_ERR_INVALID_ARG;
     if (!mirror_consistent(d, c) || !has_mirror(d, c)) return SSA_ERR_NO_MIRROR;
   }
   const WsLayout w = ws_layout(d);
@@ -366,6 +393,7 @@ static int decode_impl(const ssa_layout* lay, const ssa_cache* c, int layer0, in
   a.tickets = at<int32_t>(ws, w.tickets);
   a.status = status;
   a.host_tail = host_tail ? 1 : 0;
+  a.fetch = fetch ? 1 : 0;
   a.bt = block_table;
   cudaError_t e = launch_decode(a, (cudaStream_t)stream);
   return e == cudaSuccess ? SSA_OK : fail_cuda(e);
@@ -376,7 +404,16 @@ int ssa_sparse_paged_decode(const ssa_layout* lay, const ssa_cache* c, int layer
                             const int32_t* seq_lens, float sm_scale, void* out,
                             int32_t* status, void* ws, ssa_stream_t stream) {
   return decode_impl(lay, c, layer0, n_layers, q, sel, phys, nullptr, seq_lens, sm_scale, out,
-                     status, ws, stream);
+                     status, ws, stream, 0);
+}
+
+int ssa_sparse_paged_decode_fetch(const ssa_layout* lay, const ssa_cache* c, int layer0,
+                                  int n_layers, const void* q, const int32_t* sel,
+                                  const int32_t* phys, const int32_t* block_table,
+                                  const int32_t* seq_lens, float sm_scale, void* out,
+                                  int32_t* status, void* ws, ssa_stream_t stream) {
+  return decode_impl(lay, c, layer0, n_layers, q, sel, phys, block_table, seq_lens, sm_scale,
+                     out, status, ws, stream, 2);
 }
 
 int ssa_sparse_paged_decode_host_tail(const ssa_layout* lay, const ssa_cache* c, int layer0,
@@ -386,7 +423,7 @@ int ssa_sparse_paged_decode_host_tail(const ssa_layout* lay, const ssa_cache* c,
                                       ssa_stream_t stream) {
   if (!block_table) return SSA_ERR_INVALID_ARG;
   return decode_impl(lay, c, layer0, n_layers, q, sel, nullptr, block_table, seq_lens, sm_scale,
-                     out, status, ws, stream);
+                     out, status, ws, stream, 1);
 }
 
 const char* ssa_status_str(int code) {

@@ -80,12 +80,19 @@ constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kSmemPerCtaMax = 227 * 1024;
 constexpr int kSmemReservedPerCta = 1024;
 
+// kernel modes
+constexpr int kResident = 0;   // every selected page in its pool slot (phys)
+constexpr int kHostTail = 1;   // slots from slot_of; pages without one read from the mirror
+constexpr int kFetch = 2;      // phys marks pages bound but not copied (-2 - slot): read
+                               // from the mirror, used, and written into their slots
+
 // stage descriptor flags
 constexpr int kFirst = 1;   // first page of a piece: the stage also holds q
 constexpr int kLast = 2;    // last page of a piece: flush after it
 constexpr int kEmpty = 4;   // a piece without pages (no data in the stage)
 constexpr int kDone = 8;    // end of the CTA's range
 constexpr int kFinal = 16;  // with kLast / kEmpty: the CTA's last piece
+constexpr int kWriteBack = 32;  // fetch mode: the stage's page goes to its slot too
 
 __host__ __device__ constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -98,7 +105,7 @@ struct Cfg {
   static constexpr int kStageBytes = round_up(kQOff + kQBytes, 1024);
   static constexpr int kCombineBytes = kConsumerWarps * kMaxG * kD * 4 + 2 * kConsumerWarps * kMaxG * 4;
   // alignment slack, combine area, producer window, descriptors and barriers
-  static constexpr int kFixed = 1024 + kCombineBytes + kWindow * 8 + kMaxStages * 32 + 64;
+  static constexpr int kFixed = 1024 + kCombineBytes + kWindow * 12 + kMaxStages * 36 + 64;
   // two CTAs per SM when at least two stages fit beside the second CTA
   static constexpr int kStages2 = (kSmemPerSm / 2 - kSmemReservedPerCta - kFixed) / kStageBytes;
   static constexpr int kCtasPerSm = kStages2 >= 2 ? 2 : 1;
@@ -131,6 +138,7 @@ struct DecodeParams {
   // slot_of; pages without a slot are read from the pinned mirror over UVA
   int host_tail;
   int Lp, nmax;
+  uint8_t *k_pool, *v_pool;       // fetch mode: where fetched pages are written back
   const int32_t* bt;        // [B][nmax]
   const int32_t* slot_of;   // [Lyr][Lp]
   const uint8_t *k_mir, *v_mir;   // [Lyr][Lp][page bytes]
@@ -210,13 +218,15 @@ __device__ __forceinline__ int cta_of(const DecodeParams& p, int t) {
   return t < big ? t / (p.tq + 1) : p.tr + (t - big) / p.tq;
 }
 
-// HT: host-tail mode (pages resolved through slot_of; pages without a slot
-// read from the mirror) -- a separate instantiation, so that the resident
-// path carries none of its code
-template <bool FP8, int P, bool HT>
+// MODE: kResident, kHostTail or kFetch -- separate instantiations, so that
+// the resident path carries none of the other modes' code
+template <bool FP8, int P, int MODE>
 __global__ void __launch_bounds__(kDecodeThreads, Cfg<FP8, P>::kCtasPerSm)
 decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV) {
+  constexpr bool HT = MODE == kHostTail;
+  constexpr bool FT = MODE == kFetch;
+  constexpr bool WARP_ISSUE = HT || FT;     // pages copied by every lane of the producer
   using C = Cfg<FP8, P>;
   constexpr int NST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -227,12 +237,14 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   uint8_t* ring = smem;
   float* comb = reinterpret_cast<float*>(smem + NST * C::kStageBytes);
   int2* plist = reinterpret_cast<int2*>(smem + NST * C::kStageBytes + C::kCombineBytes);
-  int4* meta = reinterpret_cast<int4*>(plist + kWindow);                  // [NST]
+  int* pid = reinterpret_cast<int*>(plist + kWindow);                      // [kWindow] ids
+  int4* meta = reinterpret_cast<int4*>(pid + kWindow);                     // [NST]
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + NST);
   uint64_t* empty = full + NST;
   uint64_t* cfull = empty + NST;           // the consumers' states are in comb
   uint64_t* cfree = cfull + 1;             // the merge warp is done reading comb
   uint64_t* cbar = cfree + 1;              // the consumer warps' barrier (last piece)
+  int* wslot = reinterpret_cast<int*>(cbar + 1);                         // [NST] fetch mode
   __shared__ int s_abort;
   __shared__ int s_last;
 
@@ -392,7 +404,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     int st = 0;
     bool ok = true;
     int cur_row = -1, cnt = 0, seq_len = 0;
-    int pgc[4], slc[4];        // the row's first 128 entries, kept for the second pass
+    int pgc[4], slc[4], idc[4];  // the row's first 128 entries, kept for the second pass
 
     auto acquire = [&](int s) -> bool {      // lane 0: stage slot s % NST is free
       return s < NST || mbar_wait(&empty[s % NST], ((s / NST) - 1) & 1, &s_abort);
@@ -414,17 +426,25 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
 
     // one page of K and V (one KV head), its fp8 scales and, on the first
     // page of a piece, the unit's q rows.  Resident pages (ent.y >= 0, a
-    // slot) come by TMA from the pool; host-tail pages (ent.y <= -2, logical
-    // id -2 - ent.y) by 16-byte cp.async copies from the pinned mirror, every
-    // lane a share, into the same swizzled stage layout.  The whole warp.
-    auto issue_page = [&](int2 ent, int flags, int unit, int h, int layer, int seq_len) -> bool {
-      if (!(HT ? acquire_warp() : acquire(st))) return false;   // resident path: lane 0 alone
+    // slot) come by TMA from the pool; pages from the host (ent.y <= -2: in
+    // host-tail mode logical id -2 - ent.y; in fetch mode slot -2 - ent.y,
+    // logical id mid) by 16-byte cp.async copies from the pinned mirror, every
+    // lane a share, into the same swizzled stage layout, and in fetch mode
+    // marked for the consumers to write into the slot.  The whole warp in
+    // the host-tail and fetch modes, lane 0 alone in the resident mode.
+    auto issue_page = [&](int2 ent, int mid, int flags, int unit, int h, int layer,
+                          int seq_len) -> bool {
+      if (!(WARP_ISSUE ? acquire_warp() : acquire(st))) return false;
       const int sb = st % NST;
       uint8_t* stage = ring + sb * C::kStageBytes;
       const uint32_t qbytes = (flags & kFirst) ? (uint32_t)p.G * kD * 2 : 0u;
-      const bool host = HT && ent.y < 0;
-      if constexpr (HT) if (host) {
-        const size_t id = (size_t)(-2 - ent.y);
+      const bool host = WARP_ISSUE && ent.y < 0;
+      if (FT && host) {
+        flags |= kWriteBack;
+        if (lane == 0) wslot[sb] = -2 - ent.y;
+      }
+      if constexpr (WARP_ISSUE) if (host) {
+        const size_t id = (size_t)(FT ? mid : -2 - ent.y);
         const size_t pg_bytes = (size_t)p.Hkv * P * kD * (FP8 ? 1 : 2);
         const uint8_t* kpg = p.k_mir + ((size_t)layer * p.Lp + id) * pg_bytes;
         const uint8_t* vpg = p.v_mir + ((size_t)layer * p.Lp + id) * pg_bytes;
@@ -512,15 +532,26 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           sl[k] = !ok_id ? (pg[k] >= 0 ? p.S : -1) : (slot >= 0 ? slot : -2 - id[k]);
         }
       };
+      // fetch mode: the logical ids of the marked entries (pages to fetch);
+      // an out-of-range id marks the entry S (flagged, skipped)
+      auto resolve_ids = [&](const int (&pg)[4], int (&sl)[4], int (&id)[4]) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          id[k] = sl[k] <= -2 && pg[k] >= 0 && pg[k] < p.nmax ? p.bt[(size_t)b * p.nmax + pg[k]]
+                                                              : -1;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (sl[k] <= -2 && (id[k] < 0 || id[k] >= p.Lp || -2 - sl[k] >= p.S)) sl[k] = p.S;
+      };
       auto entry_valid = [&](int pg_, int sl_) -> bool {
-        return pg_ >= 0 && ((sl_ >= 0 && sl_ < p.S) || (HT && sl_ <= -2));
+        return pg_ >= 0 && ((sl_ >= 0 && sl_ < p.S) || (WARP_ISSUE && sl_ <= -2));
       };
       if (row != cur_row) {      // count the row's valid entries (once per row)
         cur_row = row;
         seq_len = p.seq_lens[b];
         cnt = 0;
         for (int base = 0; base < p.W; base += 4 * 32) {
-          int pg[4], sl[4];
+          int pg[4], sl[4], id[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {        // every load of the batch in flight at once
             const int i = base + 32 * k + lane;
@@ -528,9 +559,10 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             sl[k] = i < p.W ? phys_at(i) : -1;
           }
           if (HT) resolve(pg, sl);
+          if (FT) resolve_ids(pg, sl, id);
           if (base == 0) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) { pgc[k] = pg[k]; slc[k] = sl[k]; }
+            for (int k = 0; k < 4; ++k) { pgc[k] = pg[k]; slc[k] = sl[k]; idc[k] = FT ? id[k] : -1; }
           }
           int bad = 0;
 #pragma unroll
@@ -551,14 +583,16 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       }
       int seen = 0, issued = 0;
       for (int base = 0; base < p.W && seen < j1 && ok; base += 4 * 32) {
-        int pgv[4], slv[4];
+        int pgv[4], slv[4], idv[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int i = base + 32 * k + lane;
           pgv[k] = base == 0 ? pgc[k] : (i < p.W ? selr[i] : -1);
           slv[k] = base == 0 ? slc[k] : (i < p.W ? phys_at(i) : -1);
+          idv[k] = base == 0 ? idc[k] : -1;
         }
         if (HT && base > 0) resolve(pgv, slv);
+        if (FT && base > 0) resolve_ids(pgv, slv, idv);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           if (seen >= j1 || !ok) break;
@@ -568,17 +602,20 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           const int rank = seen + __popc(m & lt);
           const bool in = valid && rank >= j0 && rank < j1;
           const unsigned mi = __ballot_sync(0xffffffffu, in);
-          if (in) plist[__popc(mi & lt)] = make_int2(pgv[k], slv[k]);
+          if (in) {
+            plist[__popc(mi & lt)] = make_int2(pgv[k], slv[k]);
+            pid[__popc(mi & lt)] = idv[k];
+          }
           __syncwarp();
           const int nw = __popc(mi);
-          if (HT || lane == 0) {               // the resident path issues from lane 0 alone
+          if (WARP_ISSUE || lane == 0) {       // the resident path issues from lane 0 alone
             for (int x = 0; x < nw && ok; ++x, ++issued) {
               const int flags = (issued == 0 ? kFirst : 0) |
                                 (issued == j1 - j0 - 1 ? (u == u_last ? kLast | kFinal : kLast) : 0);
-              ok = issue_page(plist[x], flags, u, h, layer, seq_len);
+              ok = issue_page(plist[x], pid[x], flags, u, h, layer, seq_len);
             }
           }
-          if (!HT) ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!WARP_ISSUE) ok = __shfl_sync(0xffffffffu, ok, 0);
           __syncwarp();                        // the window is rewritten next round
           seen += __popc(m);
         }
@@ -882,6 +919,46 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       for (int bs = 0; bs < kSteps; ++bs) {
         if (((pc * kSteps + bs) & (kConsumerWarps - 1)) != warp) continue;
         const int tb0 = bs * NB * 16;
+        if (FT && (dsc.x & kWriteBack)) {
+          // fetch mode: this block's rows of the fetched page go to its slot
+          // (before any zeroing below), K, V and, from KV head 0, the scales
+          const int slot = wslot[sb];
+          const int row = dsc.z / p.Hkv, hh = dsc.z - row * p.Hkv;
+          const int layer = p.layer0 + row / p.B;
+          const size_t hp = ((size_t)layer * p.S + slot) * p.Hkv + hh;      // head-page index
+          if (FP8) {
+            uint8_t* kp = p.k_pool + hp * (P * kD);                        // [P][128]
+            uint8_t* vp = p.v_pool + hp * (P * kD);                        // [128][P]
+            for (int i = lane; i < NB * 16 * 8; i += 32) {
+              const int r = tb0 + (i >> 3), uu = i & 7;
+              *reinterpret_cast<uint4*>(kp + r * 128 + uu * 16) =
+                  *reinterpret_cast<const uint4*>(stage + r * 128 + ((uu ^ (r & 7)) << 4));
+            }
+            for (int i = lane; i < kD * NB; i += 32) {
+              const int d = i / NB, j = i - d * NB;
+              *reinterpret_cast<uint4*>(vp + d * P + tb0 + 16 * j) =
+                  *reinterpret_cast<const uint4*>(stage + C::kTileBytes +
+                                                  swz(d * P + tb0 + 16 * j, C::kVSwz));
+            }
+            if (hh == 0 && lane < 8 * NB) {
+              const int which = lane / (4 * NB), uu = lane - which * 4 * NB;
+              float* dst = const_cast<float*>(which ? p.v_scale : p.k_scale) +
+                           ((size_t)layer * p.S + slot) * P;
+              *reinterpret_cast<uint4*>(dst + tb0 + uu * 4) = *reinterpret_cast<const uint4*>(
+                  stage + 2 * C::kTileBytes + which * P * 4 + (tb0 + uu * 4) * 4);
+            }
+          } else {
+            uint8_t* kp = p.k_pool + hp * (P * kD * 2);                    // [P][256 B]
+            uint8_t* vp = p.v_pool + hp * (P * kD * 2);
+            for (int i = lane; i < 2 * NB * 16 * 16; i += 32) {
+              const int which = i / (NB * 256), rr = i - which * NB * 256;
+              const int r = tb0 + (rr >> 4), uu = rr & 15, half = uu >> 3, u8 = uu & 7;
+              *reinterpret_cast<uint4*>((which ? vp : kp) + r * 256 + uu * 16) =
+                  *reinterpret_cast<const uint4*>(stage + which * C::kTileBytes + half * (P * 128) +
+                                                  r * 128 + ((u8 ^ (r & 7)) << 4));
+            }
+          }
+        }
         // zero V of the tokens past seq_len (their bytes are not ours to trust)
         if (nvalid < tb0 + NB * 16) {
           for (int j = 0; j < NB; ++j) {
@@ -1113,14 +1190,14 @@ bool make_tmap(CUtensorMap* tm, void* base, CUtensorMapDataType dt, int esz, uin
 template <bool FP8, int P>
 size_t decode_smem() {
   using C = Cfg<FP8, P>;
-  return 1024 + (size_t)C::kStages * C::kStageBytes + C::kCombineBytes + kWindow * 8 +
-         (size_t)C::kStages * 16 + 2 * C::kStages * 8 + 4 * 8;
+  return 1024 + (size_t)C::kStages * C::kStageBytes + C::kCombineBytes + kWindow * 12 +
+         (size_t)C::kStages * 16 + 2 * C::kStages * 8 + 4 * 8 + (size_t)C::kStages * 4;
 }
 
 // CTAs of one wave: resident CTAs per SM (the configuration's target, or
 // what the occupancy calculator grants, whichever is lower) x SMs, cut so
 // that every CTA gets at least two tiles and no unit more than 130 pieces.
-template <bool FP8, int P, bool HT>
+template <bool FP8, int P, int MODE>
 int decode_grid(const Dims& d, int n_layers, int num_sms) {
   // per device: the occupancy calculator's answer depends on the GPU
   static std::atomic<int> occ_of[kMaxDevices];
@@ -1128,7 +1205,7 @@ int decode_grid(const Dims& d, int n_layers, int num_sms) {
   int occ = slot.load(std::memory_order_relaxed);
   if (occ < 1) {
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<FP8, P, HT>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<FP8, P, MODE>,
                                                       kDecodeThreads,
                                                       decode_smem<FP8, P>()) != cudaSuccess)
       o = 1;
@@ -1143,7 +1220,7 @@ int decode_grid(const Dims& d, int n_layers, int num_sms) {
   return n < 1 ? 1 : (int)n;
 }
 
-template <bool FP8, int P, bool HT>
+template <bool FP8, int P, int MODE>
 cudaError_t launch_decode_t(const DecodeArgs& a, DecodeParams& p, cudaStream_t s) {
   const Dims& d = *a.d;
   const ssa_cache& c = *a.c;
@@ -1167,10 +1244,10 @@ cudaError_t launch_decode_t(const DecodeArgs& a, DecodeParams& p, cudaStream_t s
   }
   if (!ok) return cudaErrorInvalidValue;
   const size_t smem = decode_smem<FP8, P>();
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP8, P, HT>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<FP8, P, MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int n = decode_grid<FP8, P, HT>(d, a.n_layers, a.num_sms);
+  const int n = decode_grid<FP8, P, MODE>(d, a.n_layers, a.num_sms);
   if (n > decode_max_ctas(d, a.num_sms)) return cudaErrorInvalidValue;   // workspace bound
   p.w = d.max_selected();
   const long long T = (long long)a.n_layers * d.B * d.Hkv * p.w;
@@ -1178,7 +1255,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, DecodeParams& p, cudaStream_t s
   p.T = (int)T;
   p.tq = p.T / n;
   p.tr = p.T % n;
-  e = launch_pdl(decode_kernel<FP8, P, HT>, dim3(n), dim3(kDecodeThreads), smem, s, p, tmK, tmV);
+  e = launch_pdl(decode_kernel<FP8, P, MODE>, dim3(n), dim3(kDecodeThreads), smem, s, p, tmK,
+                 tmV);
   count_launch();
   return e;
 }
@@ -1219,6 +1297,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   p.B = d.B; p.Hq = d.Hq; p.Hkv = d.Hkv; p.G = d.G; p.W = d.W; p.S = d.S;
   p.sm_log2 = a.sm_scale * 1.4426950408889634f;
   p.host_tail = a.host_tail;
+  p.k_pool = static_cast<uint8_t*>(c.k_pool);
+  p.v_pool = static_cast<uint8_t*>(c.v_pool);
   p.Lp = d.Lp;
   p.nmax = d.nmax;
   p.bt = a.bt;
@@ -1227,23 +1307,32 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   p.v_mir = static_cast<const uint8_t*>(c.v_mirror);
   p.ks_mir = c.k_scale_mirror;
   p.vs_mir = c.v_scale_mirror;
-  switch ((d.P * 2 + d.fp8) * 2 + (a.host_tail ? 1 : 0)) {
-    case 64: return launch_decode_t<false, 16, false>(a, p, s);
-    case 65: return launch_decode_t<false, 16, true>(a, p, s);
-    case 66: return launch_decode_t<true, 16, false>(a, p, s);
-    case 67: return launch_decode_t<true, 16, true>(a, p, s);
-    case 128: return launch_decode_t<false, 32, false>(a, p, s);
-    case 129: return launch_decode_t<false, 32, true>(a, p, s);
-    case 130: return launch_decode_t<true, 32, false>(a, p, s);
-    case 131: return launch_decode_t<true, 32, true>(a, p, s);
-    case 256: return launch_decode_t<false, 64, false>(a, p, s);
-    case 257: return launch_decode_t<false, 64, true>(a, p, s);
-    case 258: return launch_decode_t<true, 64, false>(a, p, s);
-    case 259: return launch_decode_t<true, 64, true>(a, p, s);
-    case 512: return launch_decode_t<false, 128, false>(a, p, s);
-    case 513: return launch_decode_t<false, 128, true>(a, p, s);
-    case 514: return launch_decode_t<true, 128, false>(a, p, s);
-    case 515: return launch_decode_t<true, 128, true>(a, p, s);
+  const int mode = a.fetch ? kFetch : (a.host_tail ? kHostTail : kResident);
+  switch ((d.P * 2 + d.fp8) * 4 + mode) {
+    case 128: return launch_decode_t<false, 16, 0>(a, p, s);
+    case 129: return launch_decode_t<false, 16, 1>(a, p, s);
+    case 130: return launch_decode_t<false, 16, 2>(a, p, s);
+    case 132: return launch_decode_t<true, 16, 0>(a, p, s);
+    case 133: return launch_decode_t<true, 16, 1>(a, p, s);
+    case 134: return launch_decode_t<true, 16, 2>(a, p, s);
+    case 256: return launch_decode_t<false, 32, 0>(a, p, s);
+    case 257: return launch_decode_t<false, 32, 1>(a, p, s);
+    case 258: return launch_decode_t<false, 32, 2>(a, p, s);
+    case 260: return launch_decode_t<true, 32, 0>(a, p, s);
+    case 261: return launch_decode_t<true, 32, 1>(a, p, s);
+    case 262: return launch_decode_t<true, 32, 2>(a, p, s);
+    case 512: return launch_decode_t<false, 64, 0>(a, p, s);
+    case 513: return launch_decode_t<false, 64, 1>(a, p, s);
+    case 514: return launch_decode_t<false, 64, 2>(a, p, s);
+    case 516: return launch_decode_t<true, 64, 0>(a, p, s);
+    case 517: return launch_decode_t<true, 64, 1>(a, p, s);
+    case 518: return launch_decode_t<true, 64, 2>(a, p, s);
+    case 1024: return launch_decode_t<false, 128, 0>(a, p, s);
+    case 1025: return launch_decode_t<false, 128, 1>(a, p, s);
+    case 1026: return launch_decode_t<false, 128, 2>(a, p, s);
+    case 1028: return launch_decode_t<true, 128, 0>(a, p, s);
+    case 1029: return launch_decode_t<true, 128, 1>(a, p, s);
+    case 1030: return launch_decode_t<true, 128, 2>(a, p, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -56,6 +56,7 @@ struct EnsureParams {
   int32_t* miss_slot;
   int32_t* n_miss;       // [n_layers]
   int32_t* phys;         // [n_layers][B][W] or null: the remapped table (a5 fused)
+  int defer;             // misses are not copied here; phys marks them -2 - slot
   int32_t* status;
   int layer0, Lp, S, B, W, nmax, N2, mstride;
   // layers whose selections one state serves: 1 (one CTA per layer), or the
@@ -333,7 +334,14 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
   }
   if (p.phys) {
     // a5 fused: every selected page of the layer now has its slot (the
-    // rebind above is visible block-wide), so translate the table here
+    // rebind above is visible block-wide), so translate the table here.
+    // With deferred fetches the pages bound by this call (the misses, ids
+    // ascending in the miss list) are marked -2 - slot: their bytes are not
+    // in the slot yet, the attention fetches them.
+    uint32_t* mids = reinterpret_cast<uint32_t*>(vic);      // free after the rebind
+    const int nm = p.defer ? m : 0;
+    for (int i = tid; i < nm; i += nt) mids[i] = (uint32_t)mpage[i];
+    if (p.defer) __syncthreads();
     int32_t* phys = p.phys + (size_t)li * BW;
     const int32_t* sel = p.sel + (size_t)li * BW;
     for (int i = tid; i < BW; i += nt) {
@@ -344,6 +352,14 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
         const int id = pg < p.nmax ? p.bt[(size_t)b * p.nmax + pg] : -1;
         if (id >= 0 && id < p.Lp) out = slot_of[id];
         if (out < 0) set_status(p.status, SSA_ST_UNRESOLVED);
+        if (out >= 0 && nm > 0) {             // binary search of id among the misses
+          int lo = 0, hi = nm;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (mids[mid] < (uint32_t)id) lo = mid + 1; else hi = mid;
+          }
+          if (lo < nm && mids[lo] == (uint32_t)id) out = -2 - out;
+        }
       }
       phys[i] = out;
     }
@@ -458,9 +474,11 @@ namespace {
 cudaError_t launch_state(const Dims& d, const ssa_cache& c, int layer0, int n_layers,
                          const int32_t* sel, int width, int preload, const int32_t* bt,
                          int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
-                         int32_t* phys, int32_t* status, cudaStream_t s, bool shared = false) {
+                         int32_t* phys, int32_t* status, cudaStream_t s, bool shared = false,
+                         bool defer = false) {
   EnsureParams p{};
   p.phys = phys;
+  p.defer = defer ? 1 : 0;
   p.nsel = shared ? n_layers : 1;
   p.slot_of = c.slot_of; p.page_of = c.page_of; p.last_use = c.last_use; p.clock = c.clock;
   p.sel = sel; p.bt = bt; p.miss_page = miss_page; p.miss_slot = miss_slot; p.n_miss = n_miss;
@@ -499,6 +517,14 @@ cudaError_t launch_ensure_state(const Dims& d, const ssa_cache& c, int layer0, i
                                 int32_t* status, cudaStream_t s) {
   return launch_state(d, c, layer0, n_layers, sel, d.W, 0, bt, miss_page, miss_slot, n_miss,
                       phys, status, s);
+}
+
+cudaError_t launch_ensure_state_deferred(const Dims& d, const ssa_cache& c, int layer0,
+                                         int n_layers, const int32_t* sel, const int32_t* bt,
+                                         int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
+                                         int32_t* phys, int32_t* status, cudaStream_t s) {
+  return launch_state(d, c, layer0, n_layers, sel, d.W, 0, bt, miss_page, miss_slot, n_miss,
+                      phys, status, s, false, true);
 }
 
 cudaError_t launch_ensure_state_shared(const Dims& d, const ssa_cache& c, int layer0,

@@ -61,6 +61,12 @@ cudaError_t launch_miss_copy(const Dims& d, const ssa_cache& c, int layer0, int 
                              const int32_t* miss_page, const int32_t* miss_slot,
                              const int32_t* n_miss, int32_t* status, cudaStream_t s,
                              bool shared = false);
+// The ensure's state update and remap with the misses' fetch left to the
+// attention: phys marks a page bound by this call as -2 - slot.
+cudaError_t launch_ensure_state_deferred(const Dims& d, const ssa_cache& c, int layer0,
+                                         int n_layers, const int32_t* sel, const int32_t* bt,
+                                         int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
+                                         int32_t* phys, int32_t* status, cudaStream_t s);
 // Residency shared by the layers of a call: one CTA ensures the union of the
 // layers' selections sel [n_layers][B][W] on layer0's state; phys for every
 // layer; the miss list [n_layers * B * W], its count n_miss[0].
@@ -90,6 +96,9 @@ struct DecodeArgs {
   // host-tail mode: phys unused; pages resolved through slot_of, those
   // without a slot read from the mirror
   int host_tail;
+  // fetch mode: phys entries -2 - slot are pages bound but not yet copied:
+  // read from the mirror, used, and written into their slots
+  int fetch;
   const int32_t* bt;  // [B][nmax]
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);

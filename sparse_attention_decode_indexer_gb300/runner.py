@@ -22,14 +22,16 @@ import math
 
 import torch
 
-from . import (KVCache, Layout, ssa_ensure_remap, ssa_ensure_remap_shared, ssa_ensure_resident,
-               ssa_index_topk, ssa_lru_init, ssa_prefetch_pages, ssa_remap_block_table,
-               ssa_sparse_paged_decode, ssa_store_kv_mirror, ssa_workspace_size)
+from . import (KVCache, Layout, ssa_ensure_remap, ssa_ensure_remap_deferred,
+               ssa_ensure_remap_shared, ssa_ensure_resident, ssa_index_topk, ssa_lru_init,
+               ssa_prefetch_pages, ssa_remap_block_table, ssa_sparse_paged_decode,
+               ssa_sparse_paged_decode_fetch, ssa_store_kv_mirror, ssa_workspace_size)
 
 
 class DecodeRunner:
     def __init__(self, layout: Layout, host_tier: bool, identity: bool, block_table, seq_lens,
-                 device="cuda", preload_width: int = 0, shared_residency: bool = False):
+                 device="cuda", preload_width: int = 0, shared_residency: bool = False,
+                 fetch_in_attention: bool = False):
         self.layout = layout
         self.cache = KVCache(layout, host_tier, device)
         L, B, W = layout.n_layers, layout.batch, layout.max_sel
@@ -54,6 +56,9 @@ class DecodeRunner:
         # one LRU state for all layers (the first layer's), each miss copied
         # for every layer; layer-batched steps only
         self.shared_residency = bool(shared_residency)
+        # misses fetched inside the attention (ssa_ensure_remap_deferred +
+        # ssa_sparse_paged_decode_fetch) instead of by a copy before it
+        self.fetch_in_attention = bool(fetch_in_attention) and host_tier
         self.preload_width = 0
         if preload_width:
             self.enable_preload(preload_width)
@@ -91,6 +96,14 @@ class DecodeRunner:
             ssa_ensure_remap_shared(c, layer0, n_layers, self.sel[sl], self.block_table,
                                     self.phys[sl], self.miss_page[sl], self.miss_slot[sl],
                                     self.n_miss[sl], self.status, self.ws)
+        elif fused and self.fetch_in_attention:
+            ssa_ensure_remap_deferred(c, layer0, n_layers, self.sel[sl], self.block_table,
+                                      self.phys[sl], self.miss_page[sl], self.miss_slot[sl],
+                                      self.n_miss[sl], self.status, self.ws)
+            ssa_sparse_paged_decode_fetch(c, layer0, n_layers, q, self.sel[sl], self.phys[sl],
+                                          self.block_table, self.seq_lens, self.sm_scale,
+                                          self.out[sl], self.status, self.ws)
+            return
         elif fused:
             ssa_ensure_remap(c, layer0, n_layers, self.sel[sl], self.block_table, self.phys[sl],
                              self.miss_page[sl], self.miss_slot[sl], self.n_miss[sl],

@@ -24,14 +24,14 @@ def oracle_state(w: wl.Workload, layers=None) -> oracle.OracleKV:
     return oracle.OracleKV(lay, host_tier=w.host_tier, identity=not w.host_tier)
 
 
-def gpu_runner(w: wl.Workload, preload_width: int = 0):
+def gpu_runner(w: wl.Workload, preload_width: int = 0, fetch_in_attention: bool = False):
     from sparse_attention_decode_indexer_gb300 import Layout
     from sparse_attention_decode_indexer_gb300.runner import DecodeRunner
     lay = Layout(w.page_size, w.n_q_heads, w.n_kv_heads, w.head_dim, w.fp8, w.n_layers,
                  w.logical_pages, w.slots, w.batch, w.pages_per_request, w.block_topk)
     return DecodeRunner(lay, host_tier=w.host_tier, identity=not w.host_tier,
                         block_table=wl.block_table(w), seq_lens=w.lens,
-                        preload_width=preload_width)
+                        preload_width=preload_width, fetch_in_attention=fetch_in_attention)
 
 
 def _u16_to_bf16(a: np.ndarray) -> torch.Tensor:
@@ -107,7 +107,7 @@ def compare_mirror(w, run, orc, l):
 
 def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
                check_pool=True, check_mirror=True, report=None, pool_every_step=True,
-               preload_width=0):
+               preload_width=0, fetch_in_attention=False):
     """Run ``steps`` decode steps of ``w`` on both sides and compare.
 
     The library always runs every layer (one launch per stage covers them
@@ -117,7 +117,7 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
     oracle_layers = list(range(w.n_layers)) if oracle_layers is None else list(oracle_layers)
     steps = w.steps if steps is None else steps
     orc = oracle_state(w)
-    run = gpu_runner(w, preload_width)
+    run = gpu_runner(w, preload_width, fetch_in_attention)
     prefill(w, run, orc, oracle_layers)
     assert int(run.status.item()) == 0, f"status {run.status.item()}"
     for l in oracle_layers:
@@ -148,7 +148,16 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
             assert nm == r["n_miss"], f"n_miss {nm} vs {r['n_miss']} layer {l} step {t}"
             assert np.array_equal(run.miss_page[l].cpu().numpy(), r["miss_page"]), "miss_page"
             assert np.array_equal(run.miss_slot[l].cpu().numpy(), r["miss_slot"]), "miss_slot"
-            assert np.array_equal(run.phys[l].cpu().numpy(), r["phys"]), f"phys layer {l} step {t}"
+            g_phys = run.phys[l].cpu().numpy()
+            if fetch_in_attention:
+                # the pages this step bound are marked -2 - slot for the attention to fetch:
+                # exactly the oracle's misses
+                marked = g_phys <= -2
+                g_phys = np.where(marked, -2 - g_phys, g_phys)
+                ids = np.where(r["sel"] >= 0, bt[np.arange(w.batch)[:, None],
+                                                 np.maximum(r["sel"], 0)], -1)
+                assert set(ids[marked].tolist()) == set(r["miss_page"][:r["n_miss"]].tolist())
+            assert np.array_equal(g_phys, r["phys"]), f"phys layer {l} step {t}"
             if preload_width:
                 g_sc = run.last_scores[l].cpu().numpy()
                 assert np.array_equal(g_sc, r["scores"]), f"preload scores layer {l} step {t}"

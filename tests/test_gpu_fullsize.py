@@ -68,3 +68,15 @@ def test_sweep_128k_full_per_layer_sizes(batch, fp8, frac):
     if frac < 1.0:
         assert rep["max_layer_misses"] >= batch * (w.block_topk + 1)   # the cold first step
     print(w.name, rep)
+
+
+@pytest.mark.parametrize("name", ["lru_pressure_64k_fp8", "host_tier_196k_fp8"])
+def test_full_size_misses_fetched_inside_the_attention(name):
+    w = wl.WORKLOADS[name]
+    if name == "host_tier_196k_fp8":
+        w = w.with_(steps=24)
+    rep = {}
+    run_parity(w, oracle_layers=[0, 5], pool_every_step=False, fetch_in_attention=True,
+               report=rep)
+    assert rep["misses"] > 0
+    print(w.name, rep)

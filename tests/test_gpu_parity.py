@@ -83,3 +83,16 @@ def test_needles_are_selected_on_both_sides():
         sel = run.sel[l].cpu().numpy()
         for b in range(w.batch):
             assert set(pages[b].tolist()) <= set(sel[b].tolist())
+
+
+HOST_TIER = [w for w in SMALL if w.host_tier]
+
+
+@pytest.mark.parametrize("w", HOST_TIER, ids=[w.name for w in HOST_TIER])
+def test_parity_misses_fetched_inside_the_attention(w):
+    # ssa_ensure_remap_deferred + ssa_sparse_paged_decode_fetch: the same
+    # state, miss lists, pool bytes (every step) and outputs as ensure + copy
+    rep = {}
+    run_parity(w, fetch_in_attention=True, report=rep)
+    assert rep["misses"] > 0
+    print(w.name, rep)

@@ -76,6 +76,7 @@ constexpr int kDecodeThreads = kConsumers + 64;
 constexpr int kMaxG = 8;
 constexpr int kWindow = 32;          // producer compaction window (entries)
 constexpr int kMaxStages = 12;
+constexpr float kSlack = 8.0f;     // log2 headroom of the running softmax reference
 constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kSmemPerCtaMax = 227 * 1024;
 constexpr int kSmemReservedPerCta = 1024;
@@ -1035,31 +1036,42 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
             if (tkB[j] >= nvalid) { x[j][2] = x[j][3] = -INFINITY; vsB[j] = 0.0f; }
           }
         }
-        // per-head maxima over the step's tokens: the 8 lanes r4 = 0..7 of c
+        // The running maximum is a reference, not the exact maximum: it moves
+        // only when a score of the step exceeds it by more than 2^kSlack, so
+        // the probabilities stay below 2^kSlack (inside the f16 and bf16
+        // operand ranges).  Only then are the exact per-head maxima reduced
+        // over the 8 lanes r4 = 0..7 of c; after the first blocks most steps
+        // skip the shuffles.  The same holds for the fp8 V-scale reference.
         float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
         for (int j = 1; j < NB; ++j) {
           mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][2]));
           mx1 = fmaxf(mx1, fmaxf(x[j][1], x[j][3]));
         }
+        float mn0 = m_run0, mn1 = m_run1, corr0 = 1.0f, corr1 = 1.0f;
+        if (__any_sync(0xffffffffu, mx0 > m_run0 + kSlack || mx1 > m_run1 + kSlack)) {
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          mn0 = fmaxf(m_run0, mx0);
+          mn1 = fmaxf(m_run1, mx1);
+          corr0 = fast_exp2(m_run0 - (mn0 == -INFINITY ? 0.0f : mn0));
+          corr1 = fast_exp2(m_run1 - (mn1 == -INFINITY ? 0.0f : mn1));
         }
-        const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
         const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
-        const float corr0 = fast_exp2(m_run0 - mu0), corr1 = fast_exp2(m_run1 - mu1);
         float oc0 = corr0, oc1 = corr1;
         float vinv = 1.0f;
         if (FP8) {
           float vmax = fmaxf(vsA[0], vsB[0]);
 #pragma unroll
           for (int j = 1; j < NB; ++j) vmax = fmaxf(vmax, fmaxf(vsA[j], vsB[j]));
+          if (__any_sync(0xffffffffu, vmax >= vref)) {
 #pragma unroll
-          for (int off = 4; off < 32; off <<= 1)
-            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
-          if (vmax >= vref) {
+            for (int off = 4; off < 32; off <<= 1)
+              vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+            // every lane holds the same tokens' scales: vmax is the step's
             const float nref = __uint_as_float(((__float_as_uint(vmax) >> 23) + 1) << 23);
             const float ratio = vref * pow2_rcp(nref);
             oc0 *= ratio;

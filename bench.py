@@ -61,8 +61,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bound on the timed oracle sample")
     ap.add_argument("--host-warmup", type=int, default=-1,
-                    help="untimed steps that warm the host tier after the prefill (-1: 40 with "
-                         "a host tier, 0 without)")
+                    help="most untimed steps that warm the host tier after the prefill, stopped "
+                         "once the ensure stage plateaus (-1: 300 with a host tier, 0 without)")
     return ap.parse_args()
 
 

@@ -794,17 +794,18 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       return ((size_t)(c_first + kk) * 2 + (kk == 0 ? slot0 : 0)) * p.G;
     };
     // thread: d = 4*lane..+3 of heads warp and warp + 4; the same merge as
-    // the merge warp's (merge_online in piece order), two pieces' loads per
-    // round trip
+    // the merge warp's (merge_online in piece order), four pieces' loads per
+    // round trip (a unit rarely spans more than four CTAs)
     const float2* pml = reinterpret_cast<const float2*>(p.part_ml);
     const float4* po = reinterpret_cast<const float4*>(p.part_o);
     float Mh[2] = {-INFINITY, -INFINITY}, Lh[2] = {0.0f, 0.0f};
     float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-    for (int k0 = 0; k0 < np; k0 += 2) {
-      float2 ml[2][2];
-      float4 x[2][2];
+    constexpr int kMB = 4;
+    for (int k0 = 0; k0 < np; k0 += kMB) {
+      float2 ml[kMB][2];
+      float4 x[kMB][2];
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
+      for (int kk = 0; kk < kMB; ++kk)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int g = warp + 4 * hh;
@@ -814,7 +815,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
+      for (int kk = 0; kk < kMB; ++kk)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) merge_online(Mh[hh], Lh[hh], acc[hh], ml[kk][hh], x[kk][hh]);
     }

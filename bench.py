@@ -95,10 +95,10 @@ def reduce_max(x: float, dist, device) -> float:
 # DRAM bytes (read + write) of one decode launch on lru_pressure_64k_fp8, from
 # the committed ncu capture of the attention kernel on that workload, valid
 # only for the kernel sources it was taken on (their SHA-256 below).
-DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53115136 + 289792,
+DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53117696 + 307456,
                   "sources": ("sparse_attention_decode_indexer_gb300/csrc/decode.cu",
                               "sparse_attention_decode_indexer_gb300/csrc/common.cuh"),
-                  "sha256": "c4aa80305fd9f4659e4cb8820dd3e4174c3cd24b33787657209f8e431a65eeff"}
+                  "sha256": "529622517bc78737c94c29ace6b62a3787489c4b0d74ab879584b54a070929c4"}
 
 
 def decode_traffic(workload_name):

@@ -534,9 +534,9 @@ def run_ours(args, rank: int, world: int, dist):
 
     # host tier: the miss fetch over the host link runs far slower in the
     # first steps after a prefill and keeps speeding up for tens of steps;
-    # untimed steps of the same query walk until it settles -- at least 50,
-    # then until the median ensure time of the last 10 steps is within 3 % of
-    # the 10 before (at most H_max) -- the count recorded in the config
+    # untimed steps of the same query walk until it settles -- at least 100,
+    # then until the median ensure time of the last 20 steps is within 3 % of
+    # the 20 before (at most H_max) -- the count recorded in the config
     H = 0
     ens_us = []
     warm_ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
@@ -545,8 +545,8 @@ def run_ours(args, rank: int, world: int, dist):
         q_cur.copy_(q_all[H])
         ens_us.append(replay_step(warm_ev)[1] * 1e3)   # the ensure_remap stage
         H += 1
-        if H >= 50:
-            last, prev = statistics.median(ens_us[-10:]), statistics.median(ens_us[-20:-10])
+        if H >= 100:
+            last, prev = statistics.median(ens_us[-20:]), statistics.median(ens_us[-40:-20])
             if last >= 0.97 * prev:
                 break
     torch.cuda.synchronize()
@@ -693,7 +693,7 @@ def run_ours(args, rank: int, world: int, dist):
                  "host_link": link,
                  "note": "the ensure_remap stage is the LRU state kernel (remap fused) plus the copy kernel",
                  "warmup_ensure_us": ({"first": ens_us[0], "step_10": ens_us[min(9, len(ens_us) - 1)],
-                                       "last_10_median": statistics.median(ens_us[-10:])}
+                                       "last_20_median": statistics.median(ens_us[-20:])}
                                       if ens_us else None)},
         "per_layer_sequential": {"value": L * w.batch * K / (sum(pl_ms) * 1e-3),
                                  "ms_per_step": statistics.mean(pl_ms),

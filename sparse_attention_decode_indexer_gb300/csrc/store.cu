@@ -72,9 +72,10 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
   uint8_t* kst = dsm + (p.fp8 ? (size_t)HD * P : 0);
   uint8_t* vst = kst + (size_t)kTokBatch * HD * esz;            // bf16 only
 
-  // the runs that start in this CTA's chunk, in token order
+  // the runs that start in this CTA's chunk, in token order (a chunk of one
+  // token: thread 0 decides alone)
   const int c0 = blockIdx.x * p.chunk, nc = min(p.chunk, p.T - c0);
-  if (tid < nc) {
+  if (tid < nc && (nc > 1 || tid == 0)) {
     const int t = c0 + tid;
     const int64_t x = p.pos[t];
     bool start = true;
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
     }
     s_start[tid] = start ? t : -1;
   }
-  __syncthreads();
+  if (nc > 1) __syncthreads();                    // nc is the same for the whole CTA
   if (tid == 0) {
     int n = 0;
     for (int i = 0; i < nc; ++i)
@@ -167,11 +168,10 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
     __syncthreads();
 
     // phase 2: codes and the slab running sum (token order), a batch of
-    // tokens at a time; K rows (bf16: and V rows) of a run of several tokens
-    // leave through shared memory as 16-byte stores, those of a run of one
-    // or two tokens (a decode-step append) straight from the registers
+    // tokens at a time; K rows (bf16: and V rows) leave through shared memory
+    // as 16-byte stores (measured faster than byte stores from the registers,
+    // one-token runs included)
     const bool full_page = (R == P);
-    const bool staged = R > 2;
     const int h = e / p.D, d = e - h * p.D;
     const int row16 = p.D * esz / 16;                  // 16-byte units per token row of a head
     for (int r0 = 0; r0 < R; r0 += kTokBatch) {
@@ -189,16 +189,10 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
         for (int i = 0; i < kTokBatch; ++i) {
           if (i >= nb) break;
           const int r = r0 + i, j = s_j[r];
-          const size_t off = ((size_t)h * P + j) * p.D + d;             // [h][j][d]
           if (p.fp8) {
             const uint8_t ck = e4m3(__bfloat162float(xk[i]) / s_ks[r]);
             const uint8_t cv = e4m3(__bfloat162float(xv[i]) / s_vs[r]);
-            if (staged) {
-              kst[(size_t)i * HD + e] = ck;
-            } else {
-              if (km) km[off] = ck;
-              if (kp) kp[off] = ck;
-            }
+            kst[(size_t)i * HD + e] = ck;
             if (full_page) {
               vt[(size_t)e * P + j] = cv;
             } else {
@@ -206,19 +200,13 @@ __global__ void __launch_bounds__(1024) store_kernel(StoreParams p) {
               if (vm) vm[offt] = cv;
               if (vp) vp[offt] = cv;
             }
-          } else if (staged) {
+          } else {
             reinterpret_cast<__nv_bfloat16*>(kst)[(size_t)i * HD + e] = xk[i];
             reinterpret_cast<__nv_bfloat16*>(vst)[(size_t)i * HD + e] = xv[i];
-          } else {
-            if (km) reinterpret_cast<__nv_bfloat16*>(km)[off] = xk[i];
-            if (kp) reinterpret_cast<__nv_bfloat16*>(kp)[off] = xk[i];
-            if (vm) reinterpret_cast<__nv_bfloat16*>(vm)[off] = xv[i];
-            if (vp) reinterpret_cast<__nv_bfloat16*>(vp)[off] = xv[i];
           }
           sum = sum + __bfloat162float(xk[i]);
         }
       }
-      if (!staged) continue;                           // R uniform: no barrier skipped unevenly
       __syncthreads();
       // token row (r, head hh): D * esz bytes at [hh][j][0..D) of the page
       const int nvec = nb * p.Hkv * row16;

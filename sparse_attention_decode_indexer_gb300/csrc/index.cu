@@ -134,14 +134,25 @@ __device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, i
   }
 
   // 3. exact int32 dot products, reduced over the lanes of each page; the
-  //    CTA walks its pages in rounds of kScoreIters groups
+  //    CTA walks its pages in rounds of kScoreIters groups.  The round's 8
+  //    page sums are reduced over the L lanes together: at each of the first
+  //    three levels a lane keeps half of its sums and trades the other half
+  //    with its partner (8 -> 4 -> 2 -> 1 sums per lane, 7 shuffles), then a
+  //    plain butterfly finishes the last log2(L) - 3 levels; lane sub ends up
+  //    with page 4*b1 + 2*b2 + b3 of the round (b1, b2, b3: its lane bits L/2,
+  //    L/4, L/8).  Integer sums: the order does not change the result.
+  static_assert(kScoreIters == 8, "the transposed reduction halves 8 sums three times");
+  const bool b1 = sub & (L >> 1), b2 = sub & (L >> 2), b3 = sub & (L >> 3);
+  const int mine = (b1 ? 4 : 0) + (b2 ? 2 : 0) + (b3 ? 1 : 0);
+  const bool writer = (sub & ((L >> 3) - 1)) == 0;
   for (int base = p0;;) {
-#pragma unroll
-    for (int it = 0; it < kScoreIters; ++it) {
+    unsigned used = 0;
+    auto dot = [&](int it) -> int {          // this lane's part of page it's score
       const int pg = base + it * groups + grp;
       const bool in = pg < p1 && pg < n_b;
       if (in && !live[it] && sub == 0) set_status(p.status, SSA_ST_BAD_ID);
       const bool use = in && live[it];
+      used |= use ? 1u << it : 0u;
       int acc = 0;
       if (use) {
 #pragma unroll
@@ -154,9 +165,24 @@ __device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, i
           }
         }
       }
-      for (int o = L >> 1; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (sub == 0 && pg < p1) out[pg] = use ? acc : INT_MIN;
+      return acc;
+    };
+    // pages i and i + 4 are scored together and traded at once, so that at
+    // most two unreduced sums are live besides the four kept ones
+    int a4[4], a2[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int lo = dot(i), hi = dot(i + 4);
+      a4[i] = (b1 ? hi : lo) + __shfl_xor_sync(0xffffffffu, b1 ? lo : hi, L >> 1);
     }
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      a2[i] = (b2 ? a4[i + 2] : a4[i]) +
+              __shfl_xor_sync(0xffffffffu, b2 ? a4[i] : a4[i + 2], L >> 2);
+    int a1 = (b3 ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, b3 ? a2[0] : a2[1], L >> 3);
+    for (int o = L >> 4; o; o >>= 1) a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    const int pg = base + mine * groups + grp;
+    if (writer && pg < p1) out[pg] = (used >> mine) & 1u ? a1 : INT_MIN;
     base += groups * kScoreIters;
     if (base >= p1) break;
     load_ids(base);

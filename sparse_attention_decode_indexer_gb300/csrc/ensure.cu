@@ -116,6 +116,42 @@ __global__ void __launch_bounds__(kEnsureThreads) ensure_state_kernel(EnsurePara
   // ids this call touches or binds
   const int32_t clock = p.clock[layer] - (p.preload ? 1 : 0);
 
+  // 0. every selected page already bound (the usual case of a resident pool):
+  //    steps 1-4 reduce to touching the hits, and a touch is the same write
+  //    whichever duplicate makes it, so one pass over the entries touches,
+  //    translates (a5 fused) and looks for a miss or a bad id.  Only if it
+  //    finds one does the full update below run; it makes the same touches
+  //    and rewrites the whole table, so nothing of this pass is lost.
+  {
+    int32_t* phys0 = p.phys ? p.phys + (size_t)li * BW : nullptr;
+    const int32_t* sel0 = p.sel + (size_t)li * BW;
+    int odd = 0;
+    for (int i = tid; i < BW; i += nt) {
+      const int b = (i / p.W) % p.B;
+      const int pg = sel0[i];
+      int out = -1;
+      if (pg >= 0) {
+        const int id = pg < p.nmax ? p.bt[(size_t)b * p.nmax + pg] : -1;
+        const int slot = id >= 0 && id < p.Lp ? slot_of[id] : -1;
+        if (slot >= 0 && slot < p.S) {
+          last_use[slot] = clock;
+          out = slot;
+        } else {
+          odd = 1;
+        }
+      }
+      if (phys0) phys0[i] = out;
+    }
+    if (!__syncthreads_or(odd)) {
+      for (int i = tid; i < p.mstride; i += nt) { mpage[i] = -1; mslot[i] = -1; }
+      if (tid == 0) {
+        p.n_miss[li] = 0;
+        if (!p.preload) p.clock[layer] = clock + 1;
+      }
+      return;
+    }
+  }
+
   // 1. the distinct selected logical ids, ascending, in ids[] (0xFFFFFFFF
   //    after them)
   auto selected_id = [&](int i) -> uint32_t {        // entry i of the batch's selection

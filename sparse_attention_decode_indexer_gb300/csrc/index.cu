@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kScoreThreads, CPL == 1 ? 3 : 2) index_score_k
 // top-k select: one CTA per (layer, request)
 // ---------------------------------------------------------------------------
 constexpr int kSelThreads = 1024;
+constexpr int kSelCand = 64;       // a bin this small is ranked directly
 // Upper bound on the static shared memory of the select (and fused index)
 // kernels: histogram, scan scratch, a few scalars.
 constexpr size_t kSelectStaticSmem = 2048;
@@ -229,7 +230,8 @@ __device__ void select_row(const int32_t* row, int n, int k, int W, int32_t* out
   __shared__ int hist[256];
   __shared__ int tmp[33];
   __shared__ uint32_t s_lo, s_hi, s_base;
-  __shared__ int s_remaining, s_shift;
+  __shared__ int s_remaining, s_shift, s_bincnt, s_ncand;
+  __shared__ uint32_t cbin[kSelCand];
   const int tid = threadIdx.x, nt = blockDim.x;
   const bool take_all = (n - 1 <= k);
   const int cand = n - 1;                // pages that compete; n-1 is forced
@@ -291,6 +293,7 @@ __device__ void select_row(const int32_t* row, int n, int k, int W, int32_t* out
               s_remaining = rem - above;
               s_base = base + (bin << shift);
               s_shift = shift;
+              s_bincnt = cnt[j];
               break;
             }
             above += cnt[j];
@@ -302,6 +305,33 @@ __device__ void select_row(const int32_t* row, int n, int k, int W, int32_t* out
       if (shift == 0) break;
       span_hi = (uint32_t)min((unsigned long long)base + ((1ull << shift) - 1ull),
                               0xFFFFFFFFull);
+      if (s_bincnt <= kSelCand) {
+        // few keys left in the bin that holds the k-th largest: rank them
+        // directly (each against all) instead of further radix passes
+        if (tid == 0) s_ncand = 0;
+        __syncthreads();
+        for (int i = tid; i < cand; i += nt) {
+          const uint32_t kk = key[i];
+          if (kk >= base && kk <= span_hi) cbin[atomicAdd(&s_ncand, 1)] = kk;
+        }
+        __syncthreads();
+        const int c = s_ncand, rem = s_remaining;
+        for (int t = tid; t < c; t += nt) {
+          const uint32_t x = cbin[t];
+          int gt = 0, eq = 0;
+          for (int j = 0; j < c; ++j) {
+            gt += cbin[j] > x;
+            eq += cbin[j] == x;
+          }
+          if (gt < rem && rem <= gt + eq) {   // x is the rem-th largest of the bin
+            s_base = x;
+            s_remaining = rem - gt;
+          }
+        }
+        __syncthreads();
+        base = s_base;
+        break;
+      }
       shift = shift >= 8 ? shift - 8 : 0;
     }
     T = base;                             // the k-th largest key

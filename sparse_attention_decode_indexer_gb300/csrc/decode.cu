@@ -666,6 +666,23 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     tauA = 4 * j + (j < 2 ? e : 2 + e);
     tauB = 4 * j + (j < 2 ? 2 + e : e);
   }
+  // fp8: the MMA fragments come from ldmatrix, lane i giving the address of
+  // row i & 7 of matrix i >> 3.  QK, per k32 step: (rows tauA, chunk 2ks),
+  // (rows tauB, 2ks), (tauA, 2ks + 1), (tauB, 2ks + 1) -- each lane gets the
+  // 4 bytes at 4c of row r4, as one 32-bit read per fragment did.  PV, per
+  // pair of 16-row d tiles: d rows 0-7 and 8-15 of the first tile, then of
+  // the second, 16 tokens each.
+  uint32_t kq_row = 0, kq_c0 = 0, kq_sw = 0, v_row = 0;
+  if (FP8) {
+    const int mi = lane >> 3, rr = lane & 7;
+    const int jj = rr >> 1, ee = rr & 1;
+    const int tA = 4 * jj + (jj < 2 ? ee : 2 + ee), tB = 4 * jj + (jj < 2 ? 2 + ee : ee);
+    const int t = (mi & 1) ? tB : tA;
+    kq_row = (uint32_t)t * 128;
+    kq_sw = (uint32_t)(t & 7);
+    kq_c0 = (uint32_t)(mi >> 1);
+    v_row = (uint32_t)(16 * (mi >> 1) + 8 * (mi & 1) + rr);
+  }
 
   // End of a piece: leave this warp's state in comb for the merge warp
   // (once it has read the previous piece's) and stream on.  The consumer
@@ -997,14 +1014,13 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
           if (FP8) {
             // A = the K codes as they are: a0/a2 = token tkA, d 32ks + 4c..+3
             // and d + 16; a1/a3 = token tkB.  hi and lo terms in two chains.
-            const uint32_t rA = kb + tkA[j] * 128 + 4 * c, rB = kb + tkB[j] * 128 + 4 * c;
-            const int xA = tkA[j] & 7, xB = tkB[j] & 7;
+            // The block's rows start at a multiple of 16 tokens, so a row's
+            // swizzle (token & 7) is the lane's constant kq_sw.
+            const uint32_t kr = kb + (uint32_t)tb * 128 + kq_row;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-              const uint32_t a0 = lds32(rA + (((2 * ks) ^ xA) << 4));
-              const uint32_t a1 = lds32(rB + (((2 * ks) ^ xB) << 4));
-              const uint32_t a2 = lds32(rA + (((2 * ks + 1) ^ xA) << 4));
-              const uint32_t a3 = lds32(rB + (((2 * ks + 1) ^ xB) << 4));
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(a0, a1, a2, a3, kr + (((2 * ks + kq_c0) ^ kq_sw) << 4));
               mma_e4m3(s4, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
               mma_e4m3(sx, a0, a1, a2, a3, qb[4 + ks][0], qb[4 + ks][1]);
             }
@@ -1119,26 +1135,26 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
 
         // O^T += V^T P^T, 16 rows of d per MMA, the step's blocks in turn
         if (FP8) {
-          // rows d = 16*mt + r4 and +8: the swizzle bits do not depend on mt
-          // (16*P*mt is a multiple of the swizzle period), so hoist them
-          uint32_t va0[NB], va1[NB];
+          // rows d = 16*mt + r4 and +8, one ldmatrix per two tiles: the
+          // swizzle bits do not depend on the tile (32*P per pair is a
+          // multiple of the swizzle period), so the lane's address is
+          // computed once per block
 #pragma unroll
           for (int j = 0; j < NB; ++j) {
-            va0[j] = vb + swz(r4 * P + tb0 + 16 * j + 4 * c, C::kVSwz);
-            va1[j] = vb + swz((r4 + 8) * P + tb0 + 16 * j + 4 * c, C::kVSwz);
-          }
+            const uint32_t va = vb + swz(v_row * P + tb0 + 16 * j, C::kVSwz);
 #pragma unroll
-          for (int j = 0; j < NB; ++j) {
+            for (int mp = 0; mp < 4; ++mp) {
+              uint32_t w[4];             // tile 2mp rows r4, r4 + 8; tile 2mp + 1 the same
+              ldsm_x4(w[0], w[1], w[2], w[3], va + mp * 32 * P);
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              uint32_t w0 = lds32(va0[j] + mt * 16 * P);
-              uint32_t w1 = lds32(va1[j] + mt * 16 * P);
-              w0 = __funnelshift_l(w0, w0, rot);
-              w1 = __funnelshift_l(w1, w1, rot);
-              uint32_t a0, a1, a2, a3;
-              e4m3x4_to_f16x2x2(w0, a0, a2);
-              e4m3x4_to_f16x2x2(w1, a1, a3);
-              mma_f16(o[mt], a0, a1, a2, a3, b0[j], b1[j]);
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t w0 = __funnelshift_l(w[2 * h], w[2 * h], rot);
+                const uint32_t w1 = __funnelshift_l(w[2 * h + 1], w[2 * h + 1], rot);
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(w0, a0, a2);
+                e4m3x4_to_f16x2x2(w1, a1, a3);
+                mma_f16(o[2 * mp + h], a0, a1, a2, a3, b0[j], b1[j]);
+              }
             }
           }
         } else {

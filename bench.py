@@ -610,6 +610,12 @@ def run_ours(args, rank: int, world: int, dist):
         out_host = torch.empty((K,) + tuple(run.out.shape), dtype=torch.bfloat16,
                                pin_memory=True)
         q_dev = torch.empty_like(q_cur)
+        # the step as a serving loop runs it: one query buffer, the step's
+        # launches captured once (on this untimed first call) and replayed
+        run.graphs = True
+        q_dev.copy_(q_host[0])
+        run.step(q_dev)
+        torch.cuda.synchronize()
         e2e_ms = []
         for t in range(K):
             flush_l2()
@@ -621,12 +627,14 @@ def run_ours(args, rank: int, world: int, dist):
             e1.record()
             e1.synchronize()
             e2e_ms.append(e0.elapsed_time(e1))
+        run.graphs = False                 # the legs below run eager steps on many q buffers
         tot = reduce_max(sum(e2e_ms) * 1e-3, dist, "cuda")
         e2e = {"value": units / tot, "unit": UNIT,
                "h2d_bytes_per_step": int(q_host[0].numel() * 2),
                "d2h_bytes_per_step": int(out_host[0].numel() * 2),
                "ms_per_step": 1e3 * tot / K,
-               "path": "DecodeRunner.step (4 C-ABI calls, direct launches) + pinned H2D q / D2H out"}
+               "path": "DecodeRunner.step (the step's C-ABI calls as one CUDA graph replay, captured "
+                       "on an untimed first call) + pinned H2D q / D2H out"}
 
     preload = host_tail = fetch = None
     if w.host_tier:

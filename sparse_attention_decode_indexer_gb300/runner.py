@@ -31,7 +31,7 @@ from . import (KVCache, Layout, ssa_ensure_remap, ssa_ensure_remap_deferred,
 class DecodeRunner:
     def __init__(self, layout: Layout, host_tier: bool, identity: bool, block_table, seq_lens,
                  device="cuda", preload_width: int = 0, shared_residency: bool = False,
-                 fetch_in_attention: bool = False):
+                 fetch_in_attention: bool = False, graphs: bool = False):
         self.layout = layout
         self.cache = KVCache(layout, host_tier, device)
         L, B, W = layout.n_layers, layout.batch, layout.max_sel
@@ -62,6 +62,9 @@ class DecodeRunner:
         self.preload_width = 0
         if preload_width:
             self.enable_preload(preload_width)
+        # layer-batched steps as CUDA graph replays, one per q buffer (see step)
+        self.graphs = bool(graphs)
+        self._graphs = {}
 
     def enable_preload(self, width: int):
         """Issue the top-k preload of `width` pages per request with every
@@ -140,13 +143,30 @@ class DecodeRunner:
     def step(self, q, per_layer: bool = False, keep_scores: bool = False):
         """q: bf16 [n_layers][B][Hq][D] on the device, all layers of the cache.
         Layer-batched steps take the ensure and the remap in one call
-        (ssa_ensure_remap); per-layer steps make the four separate calls."""
+        (ssa_ensure_remap); per-layer steps make the four separate calls.
+        With `graphs` set, a layer-batched step (without the preload) is one
+        CUDA graph replay, captured on the first call with that q buffer: a
+        serving loop that reuses its query buffer pays the launch path once."""
         L = self.layout.n_layers
         if self.preload_width and not per_layer:
             self._preload_step(q)
         elif per_layer:
             for l in range(L):
                 self._calls(q[l:l + 1], l, 1, keep_scores, fused=False)
+        elif self.graphs:
+            key = (q.data_ptr(), tuple(q.shape), keep_scores)
+            g = self._graphs.get(key)
+            if g is None:
+                # this call's step runs eagerly (and sets the kernels'
+                # attributes); the capture only records the same launches
+                self._calls(q, 0, L, keep_scores, fused=True)
+                torch.cuda.current_stream().synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    self._calls(q, 0, L, keep_scores, fused=True)
+                self._graphs[key] = g
+            else:
+                g.replay()
         else:
             self._calls(q, 0, L, keep_scores, fused=True)
         return self.out

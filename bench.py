@@ -95,10 +95,10 @@ def reduce_max(x: float, dist, device) -> float:
 # DRAM bytes (read + write) of one decode launch on lru_pressure_64k_fp8, from
 # the committed ncu capture of the attention kernel on that workload, valid
 # only for the kernel sources it was taken on (their SHA-256 below).
-DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53117696 + 307456,
+DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53118464 + 261120,
                   "sources": ("sparse_attention_decode_indexer_gb300/csrc/decode.cu",
                               "sparse_attention_decode_indexer_gb300/csrc/common.cuh"),
-                  "sha256": "529622517bc78737c94c29ace6b62a3787489c4b0d74ab879584b54a070929c4"}
+                  "sha256": "2b737158d0384bfe02d45241088c63f237f877a98d5506964111c30c8ef2abd9"}
 
 
 def decode_traffic(workload_name):

@@ -164,12 +164,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t a, int bits) {
   return a ^ (((a >> 7) & ((1u << bits) - 1u)) << 4);
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
 // 1/x for x a positive normal power of two, exactly, without a division.
 __device__ __forceinline__ float pow2_rcp(float x) {
   return __uint_as_float(0x7F000000u - __float_as_uint(x));

@@ -649,16 +649,17 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
     vref = FP8 ? 0.0f : 1.0f;
   };
   reset();
-  const int rot = c >= 2 ? 16 : 0;      // fp8 V: lanes 2, 3 hold the token pairs swapped
   // token of MMA row r4 and r4+8 within a 16-token block.  fp8: rows 2j, 2j+1
-  // and 2j+8, 2j+9 cover the 4 consecutive tokens 4j..4j+3 that one 32-bit V
-  // read returns, lanes of j >= 2 taking the pairs swapped so that the 8 rows
-  // one K read touches fall in distinct swizzle chunks (no bank conflicts)
+  // and 2j+8, 2j+9 are the 4 consecutive tokens 4j..4j+3 that one 32-bit
+  // word of a V d-row holds, in order, so the word converts straight into
+  // the PV fragment.  (Two of a K ldmatrix's 8 rows then share a swizzle
+  // chunk, a 2-way bank conflict; swapping pairs to avoid it cost a shift
+  // per V word and measured slower.)
   int tauA = r4, tauB = r4 + 8;
   if (FP8) {
     const int j = r4 >> 1, e = r4 & 1;
-    tauA = 4 * j + (j < 2 ? e : 2 + e);
-    tauB = 4 * j + (j < 2 ? 2 + e : e);
+    tauA = 4 * j + e;
+    tauB = 4 * j + 2 + e;
   }
   // fp8: the MMA fragments come from ldmatrix, lane i giving the address of
   // row i & 7 of matrix i >> 3.  QK, per k32 step: (rows tauA, chunk 2ks),
@@ -670,7 +671,7 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
   if (FP8) {
     const int mi = lane >> 3, rr = lane & 7;
     const int jj = rr >> 1, ee = rr & 1;
-    const int tA = 4 * jj + (jj < 2 ? ee : 2 + ee), tB = 4 * jj + (jj < 2 ? 2 + ee : ee);
+    const int tA = 4 * jj + ee, tB = 4 * jj + 2 + ee;
     const int t = (mi & 1) ? tB : tA;
     kq_row = (uint32_t)t * 128;
     kq_sw = (uint32_t)(t & 7);
@@ -1142,11 +1143,9 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
               ldsm_x4(w[0], w[1], w[2], w[3], va + mp * 32 * P);
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const uint32_t w0 = __funnelshift_l(w[2 * h], w[2 * h], rot);
-                const uint32_t w1 = __funnelshift_l(w[2 * h + 1], w[2 * h + 1], rot);
                 uint32_t a0, a1, a2, a3;
-                e4m3x4_to_f16x2x2(w0, a0, a2);
-                e4m3x4_to_f16x2x2(w1, a1, a3);
+                e4m3x4_to_f16x2x2(w[2 * h], a0, a2);
+                e4m3x4_to_f16x2x2(w[2 * h + 1], a1, a3);
                 mma_f16(o[2 * mp + h], a0, a1, a2, a3, b0[j], b1[j]);
               }
             }

@@ -60,6 +60,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bound on the timed oracle sample")
+    ap.add_argument("--kernel", choices=["index", "attention"], default=None,
+                    help="time one kernel alone on the workload's shape (a small pool of "
+                         "B*W slots with random contents, so that a profiler capture holds "
+                         "little device memory) instead of the step")
     ap.add_argument("--host-warmup", type=int, default=-1,
                     help="most untimed steps that warm the host tier after the prefill, stopped "
                          "once the ensure stage plateaus (-1: 300 with a host tier, 0 without)")
@@ -95,10 +99,10 @@ def reduce_max(x: float, dist, device) -> float:
 # DRAM bytes (read + write) of one decode launch on lru_pressure_64k_fp8, from
 # the committed ncu capture of the attention kernel on that workload, valid
 # only for the kernel sources it was taken on (their SHA-256 below).
-DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53118464 + 261120,
+DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53117184 + 316672,
                   "sources": ("sparse_attention_decode_indexer_gb300/csrc/decode.cu",
                               "sparse_attention_decode_indexer_gb300/csrc/common.cuh"),
-                  "sha256": "2b737158d0384bfe02d45241088c63f237f877a98d5506964111c30c8ef2abd9"}
+                  "sha256": "a0ba1c942613355b7e55a29fef272b201b7d803d2d9c0b9e188e5cb543fdea42"}
 
 
 def decode_traffic(workload_name):
@@ -1027,8 +1031,95 @@ def time_store(w: wl.Workload, run, chunk: int = 4096, n_append: int = 50):
     }
 
 
+def kernel_probe(args) -> dict:
+    """One kernel of the step alone, on the workload's shape: the indexer over
+    a random slab, or the attention over a random pool of B*W slots with k+1
+    selected pages per request (ascending, the last page included) bound to
+    slots b*W + i.  The pool is small, so an ncu capture of the launch holds
+    little device memory; the work per launch is the step's.  Returns the
+    median of --steps timed calls (after --warmup), L2 flushed before each."""
+    import torch
+    import sparse_attention_decode_indexer_gb300 as ssa
+    from sparse_attention_decode_indexer_gb300.runner import DecodeRunner
+    w = get_workload(args.workload)
+    L, B, n, P, k = w.n_layers, w.batch, w.pages_per_request, w.page_size, w.block_topk
+    W = 2 * k + 8
+    lay = ssa.Layout(P, w.n_q_heads, w.n_kv_heads, w.head_dim, w.fp8, L, B * n, B * W, B, n, k)
+    bt = torch.arange(B * n, dtype=torch.int32).reshape(B, n)
+    run = DecodeRunner(lay, host_tier=False, identity=True, block_table=bt,
+                       seq_lens=[n * P] * B)
+    c = run.cache
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+    q = torch.randn((L, B, w.n_q_heads, w.head_dim), generator=g,
+                    device="cuda").to(torch.bfloat16)
+    if args.kernel == "index":
+        c.slab.copy_(torch.randint(-127, 128, c.slab.shape, generator=g, device="cuda",
+                                   dtype=torch.int32).to(torch.int8))
+
+        def call():
+            ssa.ssa_index_topk(c, 0, L, q, run.block_table, run.seq_lens, run.sel, run.n_sel,
+                               None, run.status, run.ws)
+        nbytes = index_bytes(w)
+    else:
+        if w.fp8:
+            for pool in (c.k_pool, c.v_pool):      # finite e4m3 codes of both signs
+                codes = torch.randint(0, 126, pool.shape, generator=g, device="cuda",
+                                      dtype=torch.int32)
+                sign = torch.randint(0, 2, pool.shape, generator=g, device="cuda",
+                                     dtype=torch.int32) * 128
+                pool.copy_((codes + sign).to(torch.uint8))
+            for sc in (c.k_scale, c.v_scale):
+                sc.copy_(torch.rand(sc.shape, generator=g, device="cuda") * 0.01 + 0.001)
+        else:
+            for pool in (c.k_pool, c.v_pool):
+                pool.copy_(torch.randn(pool.numel() // 2, generator=g, device="cuda")
+                           .to(torch.bfloat16).view(torch.uint8).view(pool.shape))
+        sel = torch.full((L, B, W), -1, dtype=torch.int32)
+        phys = torch.full((L, B, W), -1, dtype=torch.int32)
+        gh = torch.Generator().manual_seed(w.seed)
+        for l in range(L):
+            for b in range(B):
+                pages = torch.randperm(n - 1, generator=gh)[:k]
+                pages = torch.sort(torch.cat([pages, torch.tensor([n - 1])])).values
+                sel[l, b, :k + 1] = pages.int()
+                phys[l, b, :k + 1] = torch.arange(b * W, b * W + k + 1, dtype=torch.int32)
+        sel, phys = sel.cuda(), phys.cuda()
+
+        def call():
+            ssa.ssa_sparse_paged_decode(c, 0, L, q, sel, phys, run.seq_lens, run.sm_scale,
+                                        run.out, run.status, run.ws)
+        nbytes = decode_bytes(w)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+    ts = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ts.append(e0.elapsed_time(e1) * 1e3)
+    st = int(run.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {ssa.status_str(st)}")
+    us = statistics.median(ts)
+    peak, kind = load_peaks()
+    return {"kernel": args.kernel, "workload": w.name, "us_per_call": us,
+            "alg_bytes": nbytes, "achieved_gbs": nbytes / (us * 1e-6) / 1e9,
+            "frac": nbytes / (us * 1e-6) / 1e9 / peak, "peak_gbs": peak, "peak_kind": kind,
+            "note": "one kernel alone on the workload's shape, random contents, small pool; "
+                    "median of the timed calls, L2 flushed before each"}
+
+
 def main():
     args = parse_args()
+    if args.kernel:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        print(json.dumps(kernel_probe(args)))
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -28,16 +28,19 @@
 //   * four consumer warps each take 16-token blocks: QK^T with the tokens as
 //     the MMA rows (A = K, B = q^T, N = 8 query heads) and PV with d as the
 //     rows (A = V^T, B = P^T, the probabilities transposed in registers by
-//     movmatrix), m16n8k16 tensor-core tiles, fp32 accumulate, online softmax
-//     in the log2 domain with warp shuffles;
-//   * bf16 K/V: bf16 MMAs, ldmatrix (V transposed by ldmatrix.trans);
-//   * fp8 K/V: the e4m3 codes convert exactly to f16, so the MMAs run in f16
-//     on the raw codes; q is scaled by a power of two into f16 range, the K
-//     scale multiplies the fp32 score, and the V scale folds into the
-//     probabilities (relative to a running power-of-two reference, so the
-//     f16 operand never overflows).  V is stored d-major in the pool
-//     ([Hkv][D][P]) so that the 8-bit reads run along tokens, the reduction
-//     axis of PV;
+//     movmatrix), fp32 accumulate, online softmax in the log2 domain against
+//     a lazy reference (the running maximum moves only when a score exceeds
+//     it by 2^8, so most blocks skip the cross-lane reductions);
+//   * bf16 K/V: m16n8k16 bf16 MMAs, fragments by ldmatrix (V transposed by
+//     ldmatrix.trans);
+//   * fp8 K/V: QK as m16n8k32 e4m3 MMAs on the raw K codes against q scaled
+//     by a power of two and split into two e4m3 terms (hi + lo); PV as
+//     m16n8k16 f16 MMAs on the V codes converted exactly to f16; fragments
+//     by ldmatrix.  The K scale multiplies the fp32 score, and the V scale
+//     folds into the probabilities (relative to a running power-of-two
+//     reference, so the f16 operand never overflows).  V is stored d-major
+//     in the pool ([Hkv][D][P]) so that the 8-bit reads run along tokens, the
+//     reduction axis of PV;
 //   * at the end of a piece each consumer warp leaves its softmax state in
 //     shared memory and streams on; a sixth warp combines the 4 states: a
 //     whole unit becomes its output, a shared unit's piece an (m, l, o)
@@ -51,9 +54,16 @@
 //     resolves each selected page through slot_of itself; a page without a
 //     slot is copied from the pinned host mirror by the producer warp's
 //     16-byte cp.async loads over UVA into the same swizzled stage layout,
-//     the stage's barrier tracking those copies instead of a TMA byte count.
+//     the stage's barrier tracking those copies instead of a TMA byte count;
+//   * fetch mode (ssa_sparse_paged_decode_fetch): entries the deferred
+//     ensure marked -2 - slot are read from the mirror the same way, and the
+//     consumer warps also write them into their slots;
+//   * the merges of a unit's pieces (by the merge warp or by the consumer
+//     warps) run the same online recurrence in piece order, so the output
+//     does not depend on which piece finishes last.
 // The work is HBM-bound (8 flop/byte bf16, 16 fp8): the tensor cores carry
-// the G-row tiles, the memory system sets the pace.
+// the G-row tiles, the memory system sets the pace where a launch is large
+// enough; the fp8 consumers' issue and ALU work limit the rest.
 #include <cudaTypedefs.h>
 #include <cuda.h>
 #include <atomic>

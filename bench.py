@@ -672,8 +672,8 @@ def run_ours(args, rank: int, world: int, dist):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": 1e3 * total_s / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 codes, f16 tensor-core MMA, f32 accumulate; int8 indexer" if w.fp8 else
-                 "bf16 tensor-core MMA, f32 accumulate; int8 indexer",
+        "dtype": "e4m3 K/V codes (QK e4m3, PV f16 tensor-core MMAs), f32 accumulate; int8 indexer"
+                 if w.fp8 else "bf16 tensor-core MMA, f32 accumulate; int8 indexer",
         "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "layers": w.n_layers, "ctx": w.ctx,
                    "page_size": w.page_size, "heads": f"{w.n_q_heads}/{w.n_kv_heads}",

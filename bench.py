@@ -102,7 +102,7 @@ def reduce_max(x: float, dist, device) -> float:
 DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53117184 + 316672,
                   "sources": ("sparse_attention_decode_indexer_gb300/csrc/decode.cu",
                               "sparse_attention_decode_indexer_gb300/csrc/common.cuh"),
-                  "sha256": "def4e5f003eacd28db7695f75be611897990d8caba1959acc06da43cbd3907e6"}
+                  "sha256": "cf58fd088b3a0ab923d6bac9fbbc65089e5a8859a6cbf766f0c40b8a182eef61"}
 
 
 def decode_traffic(workload_name):

@@ -1228,7 +1228,9 @@ size_t decode_smem() {
 
 // CTAs of one wave: resident CTAs per SM (the configuration's target, or
 // what the occupancy calculator grants, whichever is lower) x SMs, cut so
-// that every CTA gets at least two tiles and no unit more than 130 pieces.
+// that every CTA gets at least four tiles and no unit more than 130 pieces
+// (a small launch split over fewer, longer ranges merges fewer pieces per
+// unit: 27.3 -> 21.2 us for 24 units of 33 pages, the same for larger ones).
 template <bool FP8, int P, int MODE>
 int decode_grid(const Dims& d, int n_layers, int num_sms) {
   // per device: the occupancy calculator's answer depends on the GPU
@@ -1246,7 +1248,7 @@ int decode_grid(const Dims& d, int n_layers, int num_sms) {
   }
   const int w = d.max_selected();
   const long long T = (long long)n_layers * d.B * d.Hkv * w;
-  const int tpc_min = w > 256 ? (w + 127) / 128 : 2;
+  const int tpc_min = w > 256 ? (w + 127) / 128 : 4;
   long long n = T / tpc_min;
   if (n > (long long)num_sms * occ) n = (long long)num_sms * occ;
   return n < 1 ? 1 : (int)n;

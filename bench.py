@@ -99,10 +99,10 @@ def reduce_max(x: float, dist, device) -> float:
 # DRAM bytes (read + write) of one decode launch on lru_pressure_64k_fp8, from
 # the committed ncu capture of the attention kernel on that workload, valid
 # only for the kernel sources it was taken on (their SHA-256 below).
-DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53117184 + 316672,
+DECODE_TRAFFIC = {"workload": "lru_pressure_64k_fp8", "bytes": 53123328 + 245760,
                   "sources": ("sparse_attention_decode_indexer_gb300/csrc/decode.cu",
                               "sparse_attention_decode_indexer_gb300/csrc/common.cuh"),
-                  "sha256": "cf58fd088b3a0ab923d6bac9fbbc65089e5a8859a6cbf766f0c40b8a182eef61"}
+                  "sha256": "cb8879fca68c63f44cb1b94d6af4f1739193415d1ae9f92d9b2a67cc0fd12727"}
 
 
 def decode_traffic(workload_name):

@@ -939,9 +939,11 @@ decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
       // than two CTAs per SM leave, so one.
       constexpr int NB = 1;
       constexpr int kSteps = C::kBlocks / NB;
+      // this warp's blocks of the page: the stream's block index
+      // pc * kSteps + bs taken round-robin, block bs == warp - pc*kSteps mod 4
 #pragma unroll 1
-      for (int bs = 0; bs < kSteps; ++bs) {
-        if (((pc * kSteps + bs) & (kConsumerWarps - 1)) != warp) continue;
+      for (int bs = (warp - pc * kSteps) & (kConsumerWarps - 1); bs < kSteps;
+           bs += kConsumerWarps) {
         const int tb0 = bs * NB * 16;
         if (FT && (dsc.x & kWriteBack)) {
           // fetch mode: this block's rows of the fetched page go to its slot

@@ -424,7 +424,8 @@ def run_ours(args, rank: int, world: int, dist):
     W, K = args.warmup, args.steps
     H_max = args.host_warmup if args.host_warmup >= 0 else (300 if w.host_tier else 0)
     run = build_runner(w, rank, prefill_now=False)   # graphs first, then one prefill
-    n_total = H_max + W + 4 * K + (10 * K + 140 if w.host_tier else 0)
+    n_total = H_max + W + 4 * K + (10 * K + 140 + len(OVERLAP_GROUPS) * (K + 12) + 20
+                                   if w.host_tier else 0)
     q_all = queries_all(w, n_total)
     q_cur = q_all[0].clone()
     flush_w = torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB > L2
@@ -640,9 +641,10 @@ def run_ours(args, rank: int, world: int, dist):
                "path": "DecodeRunner.step (the step's C-ABI calls as one CUDA graph replay, captured "
                        "on an untimed first call) + pinned H2D q / D2H out"}
 
-    preload = host_tail = fetch = None
+    preload = host_tail = fetch = overlap = None
     if w.host_tier:
         fetch = time_fetch_in_attention(w, run, q_all, q_cur, H + W + 12 * K + 100, K, flush_l2)
+        overlap = time_overlap(w, run, q_all, q_cur, H + W + 14 * K + 130, K, flush_l2)
     if w.host_tier and not args.no_legs:
         preload = time_preload(w, run, q_all, H + W + 4 * K, K, flush_l2)
         host_tail = time_host_tail(w, run, q_all, H + W + 8 * K + 8, K, flush_l2)
@@ -719,6 +721,8 @@ def run_ours(args, rank: int, world: int, dist):
         line["store"] = store
     if fetch is not None:
         line["fetch_in_attention"] = fetch
+    if overlap is not None:
+        line["copy_attention_overlap"] = overlap
     if preload is not None:
         line["preload"] = preload
     if host_tail is not None:
@@ -783,6 +787,63 @@ def time_preload(w: wl.Workload, run, q_all, t0: int, K: int, flush_l2):
                    "stream; (a) per-step regions after an L2 flush, closed after the preload; "
                    "(b) K steps back to back")
     return out
+
+
+OVERLAP_GROUPS = (2, 4)
+
+
+def time_overlap(w: wl.Workload, run, q_all, q_cur, t0: int, K: int, flush_l2):
+    """The overlapped step (DecodeRunner overlap_groups = G: the LRU update
+    for all layers, then the host-link copy per range of layers with each
+    range's attention on a second stream behind it) for several G, timed as
+    the headline step: one CUDA graph per step with events at its ends, L2
+    flushed before each replay."""
+    import torch
+    t = t0
+    s = torch.cuda.Stream()
+    res = {}
+    for G in OVERLAP_GROUPS:
+        if G > w.n_layers:
+            continue
+        run.overlap_groups = G
+        q_cur.copy_(q_all[t]); t += 1
+        run.step(q_cur)                            # eager once, then captured
+        torch.cuda.synchronize()
+        s.wait_stream(torch.cuda.current_stream())
+        pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            pev[0].record()
+            run.step(q_cur)
+            pev[1].record()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for _ in range(10):
+            flush_l2()
+            q_cur.copy_(q_all[t]); t += 1
+            g.replay()
+        torch.cuda.synchronize()
+        ms, miss = [], 0
+        for _ in range(K):
+            flush_l2()
+            q_cur.copy_(q_all[t]); t += 1
+            g.replay()
+            pev[1].synchronize()
+            ms.append(pev[0].elapsed_time(pev[1]))
+            miss += int(run.n_miss.sum().item())
+        st = int(run.status.item())
+        if st != 0:
+            raise RuntimeError(f"device status {st} in the overlap leg (G={G})")
+        step_ms = statistics.mean(ms)
+        res[str(G)] = {"ms_per_step": step_ms, "value": w.n_layers * w.batch / (step_ms * 1e-3),
+                       "layer_groups": [n for _, n in run.layer_groups()],
+                       "misses_per_step": miss / K}
+    run.overlap_groups = 0
+    best = min(res, key=lambda k: res[k]["ms_per_step"])
+    return {"groups": res, "best": int(best),
+            "note": "ssa_ensure_remap_bind (all layers), then per layer range ssa_fetch_misses "
+                    "with that range's attention on a second stream behind it; graph per step, "
+                    "L2 flushed before each"}
 
 
 def time_fetch_in_attention(w: wl.Workload, run, q_all, q_cur, t0: int, K: int, flush_l2):

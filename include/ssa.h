@@ -254,6 +254,36 @@ int ssa_ensure_remap(const ssa_layout *lay, const ssa_cache *c, int layer0, int 
                      int32_t *status, void *ws, ssa_stream_t stream);
 
 /*
+ * ssa_ensure_remap in two calls, so that the host-link copy of one layer
+ * range can run while the attention of another range reads its pages
+ * (vLLM RFC #33980, "Motivation": the load time is what has to be hidden;
+ * FreeToken PR #499, "Design": ensure, then copy, then attend, per layer).
+ *   ssa_ensure_remap_bind: steps 1-3 and 5 of ssa_ensure_resident and the
+ *     remap of ssa_ensure_remap -- the residency state, phys and the miss
+ *     lists are final -- but nothing is copied;
+ *   ssa_fetch_misses: step 4 for the layers [layer0, layer0 + n_layers):
+ *     each listed miss's K, V (and fp8 scales) mirror -> slot.  Any split of
+ *     a bind call's range into fetch calls (lists offset to the first layer
+ *     of each) gives the bytes of the one ssa_ensure_remap call.
+ * Between the two, a missed page's slot holds stale bytes while phys already
+ * names it: the attention over a layer goes after that layer's fetch (same
+ * stream, or an event), and no other call on those layers goes between.
+ *   phys           [n_layers][B][W] int32 out (bind)
+ *   miss_page, miss_slot  [n_layers][B*W] int32, out (bind) / in (fetch)
+ *   n_miss         [n_layers] int32, out (bind) / in (fetch)
+ * The lists are required (no workspace default).  The fetch needs the host
+ * mirror (SSA_ERR_NO_MIRROR); the bind flags a miss without one on the
+ * device, as ssa_ensure_resident does.
+ */
+int ssa_ensure_remap_bind(const ssa_layout *lay, const ssa_cache *c, int layer0, int n_layers,
+                          const int32_t *sel, const int32_t *block_table, int32_t *phys,
+                          int32_t *miss_page, int32_t *miss_slot, int32_t *n_miss,
+                          int32_t *status, ssa_stream_t stream);
+int ssa_fetch_misses(const ssa_layout *lay, const ssa_cache *c, int layer0, int n_layers,
+                     const int32_t *miss_page, const int32_t *miss_slot, const int32_t *n_miss,
+                     int32_t *status, ssa_stream_t stream);
+
+/*
  * The miss fetch folded into the attention: ssa_ensure_remap_deferred runs
  * the ensure's state update and remap (a3, a5) but copies nothing; its phys
  * marks each page this call bound (a miss) as -2 - slot.  Then

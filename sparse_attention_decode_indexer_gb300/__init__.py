@@ -37,7 +37,7 @@ EXPORTS = ("ssa_workspace_size", "ssa_lru_init", "ssa_store_kv_mirror", "ssa_ind
            "ssa_index_topk_static_scratch", "ssa_selftest_bounded_wait", "ssa_host_read_probe",
            "ssa_prefetch_pages", "ssa_ensure_remap", "ssa_sparse_paged_decode_host_tail",
            "ssa_ensure_remap_shared", "ssa_ensure_remap_deferred",
-           "ssa_sparse_paged_decode_fetch")
+           "ssa_sparse_paged_decode_fetch", "ssa_ensure_remap_bind", "ssa_fetch_misses")
 
 
 class SsaError(RuntimeError):
@@ -103,6 +103,10 @@ def lib():
         L.ssa_sparse_paged_decode_fetch.restype = i32
         L.ssa_sparse_paged_decode_fetch.argtypes = ([P(SsaLayout), P(SsaCache), i32, i32, vp, vp,
                                                      vp, vp, vp, ctypes.c_float, vp, vp, vp, vp])
+        L.ssa_ensure_remap_bind.restype = i32
+        L.ssa_ensure_remap_bind.argtypes = [P(SsaLayout), P(SsaCache), i32, i32] + [vp] * 8
+        L.ssa_fetch_misses.restype = i32
+        L.ssa_fetch_misses.argtypes = [P(SsaLayout), P(SsaCache), i32, i32] + [vp] * 5
         L.ssa_ensure_remap_shared.restype = i32
         L.ssa_ensure_remap_shared.argtypes = [P(SsaLayout), P(SsaCache), i32, i32] + [vp] * 9
         L.ssa_ensure_remap.restype = i32
@@ -266,6 +270,25 @@ def ssa_ensure_remap(cache: KVCache, layer0: int, n_layers: int, sel, block_tabl
                                   n_layers, _ptr(sel), _ptr(block_table), _ptr(phys),
                                   _ptr(miss_page), _ptr(miss_slot), _ptr(n_miss), _ptr(status),
                                   _ptr(ws), _stream(stream)))
+
+
+def ssa_ensure_remap_bind(cache: KVCache, layer0: int, n_layers: int, sel, block_table, phys,
+                          miss_page, miss_slot, n_miss, status, stream=None):
+    """ssa_ensure_remap without the copy: state, phys and the miss lists are
+    final; ssa_fetch_misses copies the misses, per layer range, afterwards."""
+    _check(lib().ssa_ensure_remap_bind(ctypes.byref(cache._lay), ctypes.byref(cache.c), layer0,
+                                       n_layers, _ptr(sel), _ptr(block_table), _ptr(phys),
+                                       _ptr(miss_page), _ptr(miss_slot), _ptr(n_miss),
+                                       _ptr(status), _stream(stream)))
+
+
+def ssa_fetch_misses(cache: KVCache, layer0: int, n_layers: int, miss_page, miss_slot, n_miss,
+                     status, stream=None):
+    """Copy the listed misses of layers [layer0, layer0 + n_layers) mirror ->
+    slot; the lists are those ssa_ensure_remap_bind wrote for these layers."""
+    _check(lib().ssa_fetch_misses(ctypes.byref(cache._lay), ctypes.byref(cache.c), layer0,
+                                  n_layers, _ptr(miss_page), _ptr(miss_slot), _ptr(n_miss),
+                                  _ptr(status), _stream(stream)))
 
 
 def ssa_ensure_remap_deferred(cache: KVCache, layer0: int, n_layers: int, sel, block_table, phys,

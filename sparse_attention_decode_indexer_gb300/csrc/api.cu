@@ -256,6 +256,39 @@ int ssa_ensure_remap(const ssa_layout* lay, const ssa_cache* c, int layer0, int 
                      n_miss_opt, phys, status, ws, stream);
 }
 
+int ssa_ensure_remap_bind(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                          const int32_t* sel, const int32_t* block_table, int32_t* phys,
+                          int32_t* miss_page, int32_t* miss_slot, int32_t* n_miss,
+                          int32_t* status, ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if ((r = check_cache(d, c))) return r;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (!sel || !block_table || !phys || !miss_page || !miss_slot || !n_miss)
+    return SSA_ERR_INVALID_ARG;
+  const long long need = (long long)d.B * d.W < d.Lp ? (long long)d.B * d.W : d.Lp;
+  if (d.S < need) return SSA_ERR_POOL_TOO_SMALL;
+  cudaError_t e = launch_ensure_state(d, *c, layer0, n_layers, sel, block_table, miss_page,
+                                      miss_slot, n_miss, phys, status, (cudaStream_t)stream);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
+int ssa_fetch_misses(const ssa_layout* lay, const ssa_cache* c, int layer0, int n_layers,
+                     const int32_t* miss_page, const int32_t* miss_slot, const int32_t* n_miss,
+                     int32_t* status, ssa_stream_t stream) {
+  Dims d;
+  int r = check_layout(lay, d);
+  if (r) return r;
+  if ((r = check_cache(d, c))) return r;
+  if ((r = check_range(d, layer0, n_layers))) return r;
+  if (!miss_page || !miss_slot || !n_miss) return SSA_ERR_INVALID_ARG;
+  if (!has_mirror(d, c)) return SSA_ERR_NO_MIRROR;
+  cudaError_t e = launch_miss_copy(d, *c, layer0, n_layers, miss_page, miss_slot, n_miss, status,
+                                   (cudaStream_t)stream);
+  return e == cudaSuccess ? SSA_OK : fail_cuda(e);
+}
+
 int ssa_ensure_remap_deferred(const ssa_layout* lay, const ssa_cache* c, int layer0,
                               int n_layers, const int32_t* sel, const int32_t* block_table,
                               int32_t* phys, int32_t* miss_page_opt, int32_t* miss_slot_opt,

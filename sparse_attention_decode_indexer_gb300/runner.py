@@ -9,6 +9,15 @@ current stream.  Two launch modes:
     next layer's query depends on this layer's output must run them.
 No call synchronises the host, so a whole step can be captured in a CUDA graph.
 
+With ``overlap_groups`` = G > 1 (layer-batched steps, host tier), the ensure
+is split into its state update (ssa_ensure_remap_bind, all layers) and the
+host-link copy (ssa_fetch_misses), issued per range of layers; the attention
+over a range runs on a second stream as soon as that range's copy is done, so
+it overlaps the next range's copy.  The residency state, lists and pool bytes
+are those of the plain step; the attention splits each range's units over its
+CTAs by the range's size, so its outputs can differ from the all-layer launch
+by the rounding of a different merge order.
+
 With ``preload_width`` > 0 (layer-batched steps), every step also issues the
 top-k preload (ssa_prefetch_pages) on a second stream once its remap is done:
 the next step's likely pages are fetched while this step's attention and the
@@ -22,16 +31,18 @@ import math
 
 import torch
 
-from . import (KVCache, Layout, ssa_ensure_remap, ssa_ensure_remap_deferred,
-               ssa_ensure_remap_shared, ssa_ensure_resident, ssa_index_topk, ssa_lru_init,
-               ssa_prefetch_pages, ssa_remap_block_table, ssa_sparse_paged_decode,
-               ssa_sparse_paged_decode_fetch, ssa_store_kv_mirror, ssa_workspace_size)
+from . import (KVCache, Layout, ssa_ensure_remap, ssa_ensure_remap_bind,
+               ssa_ensure_remap_deferred, ssa_ensure_remap_shared, ssa_ensure_resident,
+               ssa_fetch_misses, ssa_index_topk, ssa_lru_init, ssa_prefetch_pages,
+               ssa_remap_block_table, ssa_sparse_paged_decode, ssa_sparse_paged_decode_fetch,
+               ssa_store_kv_mirror, ssa_workspace_size)
 
 
 class DecodeRunner:
     def __init__(self, layout: Layout, host_tier: bool, identity: bool, block_table, seq_lens,
                  device="cuda", preload_width: int = 0, shared_residency: bool = False,
-                 fetch_in_attention: bool = False, graphs: bool = False):
+                 fetch_in_attention: bool = False, graphs: bool = False,
+                 overlap_groups: int = 0):
         self.layout = layout
         self.cache = KVCache(layout, host_tier, device)
         L, B, W = layout.n_layers, layout.batch, layout.max_sel
@@ -65,6 +76,8 @@ class DecodeRunner:
         # layer-batched steps as CUDA graph replays, one per q buffer (see step)
         self.graphs = bool(graphs)
         self._graphs = {}
+        self.host_tier = bool(host_tier)
+        self.overlap_groups = int(overlap_groups)
 
     def enable_preload(self, width: int):
         """Issue the top-k preload of `width` pages per request with every
@@ -120,6 +133,47 @@ class DecodeRunner:
         ssa_sparse_paged_decode(c, layer0, n_layers, q, self.sel[sl], self.phys[sl],
                                 self.seq_lens, self.sm_scale, self.out[sl], self.status, self.ws)
 
+    def layer_groups(self):
+        """The contiguous layer ranges of an overlapped step: `overlap_groups`
+        ranges of near-equal size (the larger ones first), as (layer0, n)."""
+        L = self.layout.n_layers
+        G = max(1, min(self.overlap_groups, L))
+        sizes = [L // G + (1 if i < L % G else 0) for i in range(G)]
+        starts = [sum(sizes[:i]) for i in range(G)]
+        return list(zip(starts, sizes))
+
+    def _overlap_calls(self, q, keep_scores: bool):
+        L, c = self.layout.n_layers, self.cache
+        if not hasattr(self, "att_stream"):
+            self.att_stream = torch.cuda.Stream(device=self.sel.device)
+            self.ev_fetched = [torch.cuda.Event() for _ in range(L)]
+            self.ev_attended = torch.cuda.Event()
+        main, att = torch.cuda.current_stream(), self.att_stream
+        ssa_index_topk(c, 0, L, q, self.block_table, self.seq_lens, self.sel, self.n_sel,
+                       self.scores if keep_scores else None, self.status, self.ws)
+        ssa_ensure_remap_bind(c, 0, L, self.sel, self.block_table, self.phys, self.miss_page,
+                              self.miss_slot, self.n_miss, self.status)
+        for g, (l0, n) in enumerate(self.layer_groups()):
+            sl = slice(l0, l0 + n)
+            ssa_fetch_misses(c, l0, n, self.miss_page[sl], self.miss_slot[sl], self.n_miss[sl],
+                             self.status)
+            self.ev_fetched[g].record(main)
+            att.wait_event(self.ev_fetched[g])
+            # the attentions run one after another on att: one workspace
+            ssa_sparse_paged_decode(c, l0, n, q[sl], self.sel[sl], self.phys[sl], self.seq_lens,
+                                    self.sm_scale, self.out[sl], self.status, self.ws,
+                                    stream=att)
+        self.ev_attended.record(att)
+        main.wait_event(self.ev_attended)
+
+    def _batched_calls(self, q, keep_scores: bool):
+        overlap = (self.overlap_groups > 1 and self.host_tier and not self.shared_residency
+                   and not self.fetch_in_attention)
+        if overlap:
+            self._overlap_calls(q, keep_scores)
+        else:
+            self._calls(q, 0, self.layout.n_layers, keep_scores, fused=True)
+
     def _preload_step(self, q):
         L, c = self.layout.n_layers, self.cache
         scores = self.scores if self.n_steps % 2 == 0 else self.scores_alt
@@ -143,7 +197,10 @@ class DecodeRunner:
     def step(self, q, per_layer: bool = False, keep_scores: bool = False):
         """q: bf16 [n_layers][B][Hq][D] on the device, all layers of the cache.
         Layer-batched steps take the ensure and the remap in one call
-        (ssa_ensure_remap); per-layer steps make the four separate calls.
+        (ssa_ensure_remap), or, with `overlap_groups` > 1 on a host tier, in
+        a state call and one copy call per layer range with the attention of
+        each range overlapping the next range's copy; per-layer steps make
+        the four separate calls.
         With `graphs` set, a layer-batched step (without the preload) is one
         CUDA graph replay, captured on the first call with that q buffer: a
         serving loop that reuses its query buffer pays the launch path once."""
@@ -159,14 +216,14 @@ class DecodeRunner:
             if g is None:
                 # this call's step runs eagerly (and sets the kernels'
                 # attributes); the capture only records the same launches
-                self._calls(q, 0, L, keep_scores, fused=True)
+                self._batched_calls(q, keep_scores)
                 torch.cuda.current_stream().synchronize()
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
-                    self._calls(q, 0, L, keep_scores, fused=True)
+                    self._batched_calls(q, keep_scores)
                 self._graphs[key] = g
             else:
                 g.replay()
         else:
-            self._calls(q, 0, L, keep_scores, fused=True)
+            self._batched_calls(q, keep_scores)
         return self.out

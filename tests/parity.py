@@ -24,14 +24,16 @@ def oracle_state(w: wl.Workload, layers=None) -> oracle.OracleKV:
     return oracle.OracleKV(lay, host_tier=w.host_tier, identity=not w.host_tier)
 
 
-def gpu_runner(w: wl.Workload, preload_width: int = 0, fetch_in_attention: bool = False):
+def gpu_runner(w: wl.Workload, preload_width: int = 0, fetch_in_attention: bool = False,
+               overlap_groups: int = 0):
     from sparse_attention_decode_indexer_gb300 import Layout
     from sparse_attention_decode_indexer_gb300.runner import DecodeRunner
     lay = Layout(w.page_size, w.n_q_heads, w.n_kv_heads, w.head_dim, w.fp8, w.n_layers,
                  w.logical_pages, w.slots, w.batch, w.pages_per_request, w.block_topk)
     return DecodeRunner(lay, host_tier=w.host_tier, identity=not w.host_tier,
                         block_table=wl.block_table(w), seq_lens=w.lens,
-                        preload_width=preload_width, fetch_in_attention=fetch_in_attention)
+                        preload_width=preload_width, fetch_in_attention=fetch_in_attention,
+                        overlap_groups=overlap_groups)
 
 
 def _u16_to_bf16(a: np.ndarray) -> torch.Tensor:
@@ -107,7 +109,7 @@ def compare_mirror(w, run, orc, l):
 
 def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
                check_pool=True, check_mirror=True, report=None, pool_every_step=True,
-               preload_width=0, fetch_in_attention=False):
+               preload_width=0, fetch_in_attention=False, overlap_groups=0):
     """Run ``steps`` decode steps of ``w`` on both sides and compare.
 
     The library always runs every layer (one launch per stage covers them
@@ -117,7 +119,7 @@ def run_parity(w: wl.Workload, oracle_layers=None, steps=None, per_layer=False,
     oracle_layers = list(range(w.n_layers)) if oracle_layers is None else list(oracle_layers)
     steps = w.steps if steps is None else steps
     orc = oracle_state(w)
-    run = gpu_runner(w, preload_width, fetch_in_attention)
+    run = gpu_runner(w, preload_width, fetch_in_attention, overlap_groups)
     prefill(w, run, orc, oracle_layers)
     assert int(run.status.item()) == 0, f"status {run.status.item()}"
     for l in oracle_layers:

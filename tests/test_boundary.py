@@ -142,3 +142,32 @@ def test_more_host_side_rejections(L):
     c2.k_scale = None
     assert lib.ssa_sparse_paged_decode(ctypes.byref(lay), ctypes.byref(c2), 0, 1, p, p, p, p,
                                        0.088, p, p, p, None) == INVALID
+
+
+def test_split_ensure_host_side_rejections(L):
+    """ssa_ensure_remap_bind / ssa_fetch_misses: the lists are required, the
+    fetch needs the mirror, the layer range and the pool size are checked --
+    all on the host, before any launch."""
+    lib = L.lib()
+    p = ctypes.c_void_p(0x10000)
+    c = _fake_cache(L)
+    lay = _layout(L).c()
+    INVALID, SMALL, NO_MIRROR = -1, -2, -4
+    # bind: every list and phys required
+    for i in range(4):
+        args = [p, p, p, p]
+        args[i] = None
+        assert lib.ssa_ensure_remap_bind(ctypes.byref(lay), ctypes.byref(c), 0, 1, p, p,
+                                         args[0], args[1], args[2], args[3], p, None) == INVALID
+    # bind: the pool must hold one batch selection (80 < 2 * 72)
+    lay2 = _layout(L, batch=2, logical_pages=200, max_pages=100).c()
+    assert lib.ssa_ensure_remap_bind(ctypes.byref(lay2), ctypes.byref(c), 0, 1, p, p, p, p, p,
+                                     p, p, None) == SMALL
+    # fetch: lists required, range inside the cache, a full mirror
+    assert lib.ssa_fetch_misses(ctypes.byref(lay), ctypes.byref(c), 0, 1, None, p, p, p,
+                                None) == INVALID
+    assert lib.ssa_fetch_misses(ctypes.byref(lay), ctypes.byref(c), 1, 2, p, p, p, p,
+                                None) == INVALID
+    c2 = _fake_cache(L, mirror=False)
+    assert lib.ssa_fetch_misses(ctypes.byref(lay), ctypes.byref(c2), 0, 1, p, p, p, p,
+                                None) == NO_MIRROR

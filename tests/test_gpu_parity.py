@@ -96,3 +96,14 @@ def test_parity_misses_fetched_inside_the_attention(w):
     run_parity(w, fetch_in_attention=True, report=rep)
     assert rep["misses"] > 0
     print(w.name, rep)
+
+
+@pytest.mark.parametrize("w", HOST_TIER, ids=[w.name for w in HOST_TIER])
+def test_parity_copy_overlapped_with_attention(w):
+    # ssa_ensure_remap_bind for all layers, then per layer range
+    # ssa_fetch_misses with that range's attention on a second stream: the
+    # same state, lists, pool bytes (every step) and outputs as the oracle
+    rep = {}
+    run_parity(w, overlap_groups=w.n_layers, report=rep)
+    assert rep["misses"] > 0
+    print(w.name, rep)

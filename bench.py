@@ -644,8 +644,8 @@ def run_ours(args, rank: int, world: int, dist):
     preload = host_tail = fetch = overlap = None
     if w.host_tier:
         fetch = time_fetch_in_attention(w, run, q_all, q_cur, H + W + 12 * K + 100, K, flush_l2)
-        overlap = time_overlap(w, run, q_all, q_cur, H + W + 14 * K + 130, K, flush_l2)
     if w.host_tier and not args.no_legs:
+        overlap = time_overlap(w, run, q_all, q_cur, H + W + 14 * K + 130, K, flush_l2)
         preload = time_preload(w, run, q_all, H + W + 4 * K, K, flush_l2)
         host_tail = time_host_tail(w, run, q_all, H + W + 8 * K + 8, K, flush_l2)
     if rank != 0:

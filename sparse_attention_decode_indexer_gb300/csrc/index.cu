@@ -66,17 +66,22 @@ __device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, i
   }
   int4 v[kScoreIters][CPL];
   bool live[kScoreIters];          // a slab row was loaded (the id is in range)
-  int ids[kScoreIters];
+  // a round's block-table ids: lane sub < kScoreIters of each page group
+  // loads the id of the group's page sub of the round (one register), and
+  // the round's loads take them by shuffles within the group; the next
+  // round's ids are loaded while this round is scored
+  static_assert(kScoreIters <= 8, "the lanes of a page group hold a round's ids");
+  int id_lane = -1;
   auto load_ids = [&](int base) {
-#pragma unroll
-    for (int it = 0; it < kScoreIters; ++it) {
-      const int pg = base + it * groups + grp;
-      ids[it] = pg < p1 ? p.bt[(size_t)b * p.nmax + pg] : -1;
-    }
+    const int pg = base + (sub & (kScoreIters - 1)) * groups + grp;
+    id_lane = sub < kScoreIters && pg < p1 ? p.bt[(size_t)b * p.nmax + pg] : -1;
   };
+  int ids[kScoreIters];
   // the slab loads wait only for the ids (not for seq_len): a page past the
   // request's length is masked, and a bad id flagged, when it is scored
   auto load_round = [&](int base) {
+#pragma unroll
+    for (int it = 0; it < kScoreIters; ++it) ids[it] = __shfl_sync(0xffffffffu, id_lane, it, L);
 #pragma unroll
     for (int it = 0; it < kScoreIters; ++it) {
       const int pg = base + it * groups + grp;
@@ -147,6 +152,7 @@ __device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, i
   const bool writer = (sub & ((L >> 3) - 1)) == 0;
   for (int base = p0;;) {
     unsigned used = 0;
+    if (base + groups * kScoreIters < p1) load_ids(base + groups * kScoreIters);
     auto dot = [&](int it) -> int {          // this lane's part of page it's score
       const int pg = base + it * groups + grp;
       const bool in = pg < p1 && pg < n_b;
@@ -185,7 +191,6 @@ __device__ __forceinline__ void score_chunk(const ScoreParams& p, int16_t* qg, i
     if (writer && pg < p1) out[pg] = (used >> mine) & 1u ? a1 : INT_MIN;
     base += groups * kScoreIters;
     if (base >= p1) break;
-    load_ids(base);
     load_round(base);
   }
 }

@@ -38,6 +38,15 @@ from . import (KVCache, Layout, ssa_ensure_remap, ssa_ensure_remap_bind,
                ssa_store_kv_mirror, ssa_workspace_size)
 
 
+def split_layers(n_layers: int, groups: int):
+    """`groups` contiguous ranges of near-equal size covering [0, n_layers),
+    the larger ones first, as (layer0, n); groups is clamped to [1, n_layers]."""
+    G = max(1, min(int(groups), n_layers))
+    sizes = [n_layers // G + (1 if i < n_layers % G else 0) for i in range(G)]
+    starts = [sum(sizes[:i]) for i in range(G)]
+    return list(zip(starts, sizes))
+
+
 class DecodeRunner:
     def __init__(self, layout: Layout, host_tier: bool, identity: bool, block_table, seq_lens,
                  device="cuda", preload_width: int = 0, shared_residency: bool = False,
@@ -134,13 +143,8 @@ class DecodeRunner:
                                 self.seq_lens, self.sm_scale, self.out[sl], self.status, self.ws)
 
     def layer_groups(self):
-        """The contiguous layer ranges of an overlapped step: `overlap_groups`
-        ranges of near-equal size (the larger ones first), as (layer0, n)."""
-        L = self.layout.n_layers
-        G = max(1, min(self.overlap_groups, L))
-        sizes = [L // G + (1 if i < L % G else 0) for i in range(G)]
-        starts = [sum(sizes[:i]) for i in range(G)]
-        return list(zip(starts, sizes))
+        """The contiguous layer ranges of an overlapped step, as (layer0, n)."""
+        return split_layers(self.layout.n_layers, self.overlap_groups)
 
     def _overlap_calls(self, q, keep_scores: bool):
         L, c = self.layout.n_layers, self.cache

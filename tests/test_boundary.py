@@ -171,3 +171,64 @@ def test_split_ensure_host_side_rejections(L):
     c2 = _fake_cache(L, mirror=False)
     assert lib.ssa_fetch_misses(ctypes.byref(lay), ctypes.byref(c2), 0, 1, p, p, p, p,
                                 None) == NO_MIRROR
+
+
+def test_variant_calls_host_side_rejections(L):
+    """The documented host-side rejections of the step's variant calls (fused
+    ensure, deferred ensure and fetch-mode attention, host-tail attention,
+    shared residency, top-k preload, the static-scratch indexer, the host-link
+    probe), each returned before any launch."""
+    lib = L.lib()
+    p = ctypes.c_void_p(0x10000)
+    c = _fake_cache(L)
+    nomir = _fake_cache(L, mirror=False)
+    lay = _layout(L).c()
+    INVALID, UNSUPPORTED, NO_MIRROR, SCRATCH = -1, -3, -4, -6
+    by = ctypes.byref
+    # the fused ensure needs phys
+    assert lib.ssa_ensure_remap(by(lay), by(c), 0, 1, p, p, None, p, p, p, p, p, None) == INVALID
+    # deferred ensure: phys required, and the attention will fetch from the mirror
+    assert lib.ssa_ensure_remap_deferred(by(lay), by(c), 0, 1, p, p, None, p, p, p, p, p,
+                                         None) == INVALID
+    assert lib.ssa_ensure_remap_deferred(by(lay), by(nomir), 0, 1, p, p, p, p, p, p, p, p,
+                                         None) == NO_MIRROR
+    # fetch-mode attention: block table and mirror required
+    assert lib.ssa_sparse_paged_decode_fetch(by(lay), by(c), 0, 1, p, p, p, None, p, 0.088, p,
+                                             p, p, None) == INVALID
+    assert lib.ssa_sparse_paged_decode_fetch(by(lay), by(nomir), 0, 1, p, p, p, p, p, 0.088, p,
+                                             p, p, None) == NO_MIRROR
+    # host-tail attention: block table, slot_of and mirror required
+    assert lib.ssa_sparse_paged_decode_host_tail(by(lay), by(c), 0, 1, p, p, None, p, 0.088, p,
+                                                 p, p, None) == INVALID
+    assert lib.ssa_sparse_paged_decode_host_tail(by(lay), by(nomir), 0, 1, p, p, p, p, 0.088, p,
+                                                 p, p, None) == NO_MIRROR
+    noslot = _fake_cache(L)
+    noslot.slot_of = None
+    assert lib.ssa_sparse_paged_decode_host_tail(by(lay), by(noslot), 0, 1, p, p, p, p, 0.088,
+                                                 p, p, p, None) == INVALID
+    # shared residency: the union of a call's selections is sorted in shared
+    # memory, at most 16,384 entries (2 layers x 128 requests x 72 > 16,384)
+    big = _layout(L, batch=128, logical_pages=20000, pool_slots=20000, max_pages=100).c()
+    assert lib.ssa_ensure_remap_shared(by(big), by(c), 0, 2, p, p, p, p, p, p, p, p,
+                                       None) == UNSUPPORTED
+    assert lib.ssa_ensure_remap_shared(by(lay), by(c), 0, 1, p, p, None, p, p, p, p, p,
+                                       None) == INVALID
+    # top-k preload: width in [1, max_sel], scores and a workspace required
+    for width in (0, 73):
+        assert lib.ssa_prefetch_pages(by(lay), by(c), 0, 1, p, p, p, width, p, p, p, p, p,
+                                      None) == INVALID, width
+    assert lib.ssa_prefetch_pages(by(lay), by(c), 0, 1, None, p, p, 8, p, p, p, p, p,
+                                  None) == INVALID
+    assert lib.ssa_prefetch_pages(by(lay), by(c), 0, 1, p, p, p, 8, p, p, p, p, None,
+                                  None) == INVALID
+    # the static-scratch indexer: n_layers * batch * max_pages above its scratch
+    huge = _layout(L, n_layers=2, batch=64, logical_pages=64 * 10000, pool_slots=64 * 72,
+                   max_pages=10000).c()
+    assert lib.ssa_workspace_size(by(huge)) > 0          # a layout the library accepts
+    assert lib.ssa_index_topk_static_scratch(by(huge), by(c), 0, 2, p, p, p, p, p, p,
+                                             None) == SCRATCH
+    # the host-link probe: aligned buffers, chunk a multiple of 16 bytes, 4/8/16 loads
+    assert lib.ssa_host_read_probe(p, p, p, 4, 24, 8, None) == INVALID
+    assert lib.ssa_host_read_probe(p, p, p, 4, 4096, 6, None) == INVALID
+    assert lib.ssa_host_read_probe(ctypes.c_void_p(0x10008), p, p, 4, 4096, 8, None) == INVALID
+    assert lib.ssa_host_read_probe(p, p, p, 0, 4096, 8, None) == INVALID
